@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+slot mapping -> KV-cache write of the step's new tokens -> paged attention
+(decode: split-KV kernel + reduce; mixed batches: decode rows plus prefill
+chunks).  The default workload is the batch-256 GQA decode configuration
+(32 q-heads / 8 kv-heads, head_dim 128, bf16, block size 16, context lengths
+from a power law x^-1.2 on [16, 4096], 64 sequences sharing a 1024-token
+prefix).
+
+Metric: paged-decode KV GB/s = algorithmic bytes of the step (unique KV
+bytes, q and out, the new K/V rows read and written, table entries) divided
+by the step's device time; attention tokens/s is reported beside it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica (no collective on the data
+path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from pagedattention_kv_cache_reshape_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged-decode KV GB/s (% of GB300 HBM peak) and attention tokens/s per step"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="gqa256_bf16", choices=list(W.FULL_CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true", help="launch each step's kernels directly")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_bytes(w: W.Workload):
+    """Algorithmic bytes of one step, split by part."""
+    eb = w.k_cache.element_size()
+    ctx = w.context_lens.cpu().numpy().astype(np.int64)
+    row = w.num_kv_heads * w.head_dim * eb                      # one token, all kv-heads, K or V
+    logical_tokens = int(ctx.sum())
+    shared = max(w.shared_prefix_seqs - 1, 0) * w.shared_prefix_blocks * w.block_size
+    unique_tokens = logical_tokens - shared
+    q_bytes = w.total_q * w.num_heads * w.head_dim * eb
+    nb = int(sum(w.blocks_per_seq))
+    meta = nb * 4 + w.num_seqs * 4 * 3 + w.total_q * 8 * 2     # table entries, lengths, slots w+r
+    new_kv = w.total_q * row * 2 * 2                              # K,V rows read and written
+    return dict(kv_unique=unique_tokens * row * 2, kv_logical=logical_tokens * row * 2,
+                q=q_bytes, out=q_bytes, new_kv=new_kv, meta=meta,
+                unique_tokens=unique_tokens, logical_tokens=logical_tokens)
+
+
+def prefill_flops(w: W.Workload):
+    ql = w.q_lens
+    ctx = w.context_lens.cpu().numpy()
+    f = 0
+    for q, c in zip(ql, ctx):
+        if q > 1:
+            pos = np.arange(c - q, c) + 1                 # keys visible to each query row
+            f += int(4 * w.num_heads * w.head_dim * pos.sum())
+    return f
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "100"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) sample
+
+def oracle_sample(w_cpu: W.Workload, budget_s: float, nthreads: int):
+    """Times the oracle, as it stands, on a prefix of the workload's sequences
+    sized to about `budget_s`.  Returns (bytes_per_s, seconds, description)."""
+    import oracle as O
+
+    def sub(n):
+        cu = w_cpu.cu_seqlens_q[:n + 1]
+        rows = int(cu[-1])
+        return W.Workload(
+            name=w_cpu.name, dtype=w_cpu.dtype, num_heads=w_cpu.num_heads, num_kv_heads=w_cpu.num_kv_heads,
+            head_dim=w_cpu.head_dim, block_size=w_cpu.block_size, num_blocks=w_cpu.num_blocks,
+            max_blocks=w_cpu.max_blocks, block_tables=w_cpu.block_tables[:n].contiguous(),
+            context_lens=w_cpu.context_lens[:n].contiguous(), seq_start=w_cpu.seq_start[:n].contiguous(),
+            cu_seqlens_q=cu.contiguous(), q=w_cpu.q[:rows].contiguous(), key=w_cpu.key[:rows].contiguous(),
+            value=w_cpu.value[:rows].contiguous(), k_cache=w_cpu.k_cache, v_cache=w_cpu.v_cache,
+            scale=w_cpu.scale, shared_prefix_seqs=min(w_cpu.shared_prefix_seqs, n),
+            shared_prefix_blocks=w_cpu.shared_prefix_blocks, blocks_per_seq=w_cpu.blocks_per_seq[:n])
+
+    def run(ws):
+        t0 = time.perf_counter()
+        slots = O.slot_mapping(ws.block_tables, ws.seq_start, ws.cu_seqlens_q, ws.block_size, ws.num_blocks)
+        O.reshape_and_cache(ws.key, ws.value, ws.k_cache, ws.v_cache, slots, ws.block_size)
+        O.paged_attention(ws.q, ws.k_cache, ws.v_cache, ws.block_tables, ws.context_lens, ws.scale,
+                          cu_seqlens_q=None if ws.decode_only else ws.cu_seqlens_q, nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    n = 1
+    t = run(sub(n))
+    while n < w_cpu.num_seqs and t < budget_s / 4:
+        n = min(w_cpu.num_seqs, max(n + 1, int(n * min(8.0, budget_s / max(t, 1e-3) / 2))))
+        t = run(sub(n))
+    ws = sub(n)
+    b = workload_bytes(ws)
+    total = b["kv_unique"] + b["q"] + b["out"] + b["new_kv"] + b["meta"]
+    desc = (f"first {n} of {w_cpu.num_seqs} sequences of {w_cpu.name} (seed-identical inputs), "
+            f"slot mapping + cache write + attention, fp64 oracle, {nthreads} threads")
+    return total / t, t, desc, n, ws
+
+
+# ------------------------------------------------------------------ our path
+
+def run_ours(args, world, rank, local):
+    from pagedattention_kv_cache_reshape_gb300 import build, pa
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    pa.load()
+    w = W.make(args.config, args.seed + rank, pa.num_blocks_needed, device=dev)
+    decode_only = w.decode_only
+    max_q = int(w.q_lens.max())
+    slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
+    out = torch.empty_like(w.q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = (pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                         w.block_size, w.max_blocks) if decode_only else
+                pa.varlen_prefill_workspace_size(w.num_seqs, w.total_q, w.num_heads, w.num_kv_heads,
+                                                 w.head_dim, w.block_size, w.max_blocks))
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q=w.q, key=w.key, value=w.value, bt=w.block_tables, ctx=w.context_lens,
+             ss=w.seq_start, cu=w.cu_seqlens_q, o=out):
+        pa.compute_slot_mapping(bt, ss, cu, w.num_blocks, w.total_q, slot_mapping=slots,
+                                dev_status=status, stream=stream)
+        pa.reshape_and_cache(key, value, w.k_cache, w.v_cache, slots, dev_status=status, stream=stream)
+        if decode_only:
+            pa.decode(q, w.k_cache, w.v_cache, bt, ctx, w.scale, out=o, workspace=workspace,
+                      dev_status=status, stream=stream)
+        else:
+            pa.varlen_prefill(q, cu, w.k_cache, w.v_cache, bt, ctx, w.scale, max_q, out=o,
+                              workspace=workspace, dev_status=status, stream=stream)
+
+    launches_per_step = 2 + 3 + (0 if decode_only else 1)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st = pa.get_device_status(status)
+    if st != 0:
+        raise RuntimeError(f"device status {pa.status_string(st)} during warm-up")
+
+    graph = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            stream_saved = stream
+            pa_stream = side
+
+            def cap_step():
+                pa.compute_slot_mapping(w.block_tables, w.seq_start, w.cu_seqlens_q, w.num_blocks,
+                                        w.total_q, slot_mapping=slots, dev_status=status, stream=pa_stream)
+                pa.reshape_and_cache(w.key, w.value, w.k_cache, w.v_cache, slots, dev_status=status,
+                                     stream=pa_stream)
+                if decode_only:
+                    pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, out=out,
+                              workspace=workspace, dev_status=status, stream=pa_stream)
+                else:
+                    pa.varlen_prefill(w.q, w.cu_seqlens_q, w.k_cache, w.v_cache, w.block_tables,
+                                      w.context_lens, w.scale, max_q, out=out, workspace=workspace,
+                                      dev_status=status, stream=pa_stream)
+            cap_step()
+            side.synchronize()
+            with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+                cap_step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = g
+
+    flush = torch.empty(2 * L2_BYTES // 4 * 2, dtype=torch.float32, device=dev)   # ~258 MB > L2
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in kev:
+        a.record(); b.record()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            if graph is not None:
+                ev[i][0].record(stream)
+                graph.replay()
+                ev[i][1].record(stream)
+            else:
+                pa.set_timing_events(*kev[i])
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    pa.set_timing_events(None, None)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = float(sum(step_ms))
+
+    # dominant kernel on its own: the main attention kernel, timed by events the
+    # library records around that launch on the launching stream (direct launches)
+    kern_ms = []
+    for i in range(min(K, 100)):
+        flush.zero_()
+        pa.set_timing_events(*kev[i])
+        step()
+    pa.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_time(b) for a, b in kev[:min(K, 100)]]
+    st = pa.get_device_status(status)
+    if st != 0:
+        raise RuntimeError(f"device status {pa.status_string(st)} in the timed region")
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(w, k).cpu().pin_memory() for k in
+                ("q", "key", "value", "block_tables", "context_lens", "seq_start", "cu_seqlens_q")}
+        devb = {k: torch.empty_like(getattr(w, k)) for k in host}
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        K2 = min(K, 100)
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+        for i in range(K2 + 3):
+            flush.zero_()
+            if i >= 3:
+                e_ev[i - 3][0].record(stream)
+            for k in host:
+                devb[k].copy_(host[k], non_blocking=True)
+            step(q=devb["q"], key=devb["key"], value=devb["value"], bt=devb["block_tables"],
+                 ctx=devb["context_lens"], ss=devb["seq_start"], cu=devb["cu_seqlens_q"], o=out)
+            out_host.copy_(out, non_blocking=True)
+            if i >= 3:
+                e_ev[i - 3][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
+        e2e = (e2e_ms, h2d, d2h)
+
+    return dict(w=w, total_ms=total_ms, step_ms=step_ms, kern_ms=kern_ms, clocks=clk.summary(),
+                graph=graph is not None, launches=launches_per_step * K, e2e=e2e, wall=t_wall)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        return main_reference(args, world, rank)
+
+    r = run_ours(args, world, rank, local)
+    w = r["w"]
+    b = workload_bytes(w)
+    step_bytes = b["kv_unique"] + b["q"] + b["out"] + b["new_kv"] + b["meta"]
+    total_s = r["total_ms"] / 1e3
+    # whole job: units of all ranks over the slowest rank's time
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_s, float(step_bytes)], device="cuda")
+        tmax = t.clone()
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        tsum = t.clone()
+        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+        total_s = float(tmax[0])
+        job_bytes = float(tsum[1]) * args.steps
+    else:
+        job_bytes = float(step_bytes) * args.steps
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    K = args.steps
+    gbs = job_bytes / total_s / 1e9
+    ms_per_step = r["total_ms"] / K
+    peak, peak_kind = measured_peaks()
+    kern_ms = float(np.mean(r["kern_ms"]))
+    kern_bytes = b["kv_unique"] + b["q"] + b["out"]
+    achieved = kern_bytes / (kern_ms / 1e3) / 1e9
+    traffic = read_profile_traffic(args.config)
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) values, power-law lengths, shuffled block pool)",
+        "config": {
+            "workload": w.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "num_blocks": w.num_blocks, "context_tokens": b["logical_tokens"],
+            "unique_context_tokens": b["unique_tokens"], "query_tokens": w.total_q,
+            "l2": "flushed before every timed step (258 MB write)",
+            "launch": "CUDA graph of the step's kernels" if r["graph"] else "direct launches",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "tokens_per_s": round(world * w.total_q * K / total_s, 1),
+        "kv_gbs_logical": round(b["kv_logical"] * K * world / total_s / 1e9, 2),
+        "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * gbs / world / 8000.0, 2),
+        "roofline": {
+            "kernel": "split_decode_kernel",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "traffic": traffic, "bytes_per_launch": kern_bytes, "avg_launch_ms": round(kern_ms, 5),
+        },
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if r["e2e"] is not None:
+        e2e_ms, h2d, d2h = r["e2e"]
+        line["e2e"] = {"value": round(step_bytes / (e2e_ms / 1e3) / 1e9 * world, 2), "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_ms, 5)}
+    if not w.decode_only:
+        line["prefill_flops_per_step"] = prefill_flops(w)
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle as O
+        nthreads = os.cpu_count() or 1
+        bps, secs, desc, n, _ = oracle_sample(w.to("cpu"), args.cpu_seconds, nthreads)
+        line["cpu_baseline"] = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": nthreads,
+                                "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def read_profile_traffic(config):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    if one exists for this workload and kernel build; else None."""
+    path = os.path.join(ROOT, "profiles", f"split_decode_kernel_{config}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha") != kernel_source_sha():
+            return None
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    p = os.path.join(ROOT, "pagedattention_kv_cache_reshape_gb300", "csrc", "attn_decode.cu")
+    with open(p, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def main_reference(args, world, rank):
+    """The oracle as it stands on the host cores, on the same workload."""
+    if rank != 0:
+        return
+    import oracle as O
+    O.build()
+    w = W.make(args.config, args.seed, O.num_blocks_needed, device="cpu")
+    nthreads = os.cpu_count() or 1
+    per_step = max(0.05, 150.0 / max(args.steps + args.warmup, 1))
+    # size one step's sample once, then time K steps of it
+    _, _, desc, n, ws = oracle_sample(w, per_step, nthreads)
+    b = workload_bytes(ws)
+    step_bytes = b["kv_unique"] + b["q"] + b["out"] + b["new_kv"] + b["meta"]
+
+    def one():
+        t0 = time.perf_counter()
+        slots = O.slot_mapping(ws.block_tables, ws.seq_start, ws.cu_seqlens_q, ws.block_size, ws.num_blocks)
+        O.reshape_and_cache(ws.key, ws.value, ws.k_cache, ws.v_cache, slots, ws.block_size)
+        O.paged_attention(ws.q, ws.k_cache, ws.v_cache, ws.block_tables, ws.context_lens, ws.scale,
+                          cu_seqlens_q=None if ws.decode_only else ws.cu_seqlens_q, nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one()
+    times = [one() for _ in range(args.steps)]
+    total = sum(times)
+    gbs = step_bytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) values, power-law lengths, shuffled block pool)",
+        "config": {"workload": w.name, "sample_sequences": n, "num_seqs": w.num_seqs},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged KV-cache library: slot mapping,
+ * KV-cache write ("reshape_and_cache"), paged decode attention with a split-KV
+ * reduction, and varlen paged prefill over a mixed prefill + decode batch.
+ *
+ * Sources for what each call computes (page title, section):
+ *  [iitog] "vLLM изнутри: как устроен движок для быстрого инференса LLM":
+ *          allocate_slots paragraph (blocks of 16 tokens, ceil(17/16) = 2);
+ *          model-runner paragraph (slot map built while preparing inputs; the
+ *          batch is one concatenated super-sequence in which masks and
+ *          positions keep every sequence on its own tokens; prefill is
+ *          compute-bound, decode reads earlier tokens' KV from the cache and
+ *          is memory-bound).
+ *  [kwkr]  "vLLM：颠覆大模型推理的高效API服务引擎深度解析": §1.2 (fixed-size
+ *          blocks, per-request block table from logical to physical blocks),
+ *          §1.3 (one pre-allocated pool shared by all requests; a new token's
+ *          K/V vectors are stored into its physical block; attention gathers
+ *          the scattered blocks into a logically contiguous KV through the
+ *          block table; blocks may be referenced read-only by several block
+ *          tables, e.g. a shared system prompt).
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, except the
+ *    host output of pa_get_device_status.  The library never allocates or
+ *    frees device memory; scratch comes from the caller's `workspace`, sized
+ *    by the matching *_workspace_size call.
+ *  - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  Only pa_get_device_status synchronises.
+ *  - Argument errors are found on the host before any launch and returned
+ *    as a pa_status; nothing is launched then.
+ *  - Data-dependent range errors (a block id outside [0, num_blocks), a slot
+ *    outside the pool, a context length <= 0 or beyond max_blocks*block_size)
+ *    are recorded into *dev_status (when dev_status != NULL) as
+ *    PA_ERR_OUT_OF_RANGE by the first failing thread; the offending element
+ *    is skipped, no out-of-bounds access is made and nothing traps.  Rows of
+ *    `out` whose sequence had such an error are unspecified (a context length
+ *    error leaves the row untouched).  A bounded wait inside a kernel that
+ *    runs out records PA_ERR_TIMEOUT the same way.
+ *  - Layouts (all row-major, contiguous unless a stride is given):
+ *      pools        k_cache, v_cache: [num_blocks][block_size][num_kv_heads][head_dim]
+ *      block_tables int32 [num_seqs][max_blocks]; entries past a sequence's
+ *                   last block are never read
+ *      q, out       [rows][num_heads][head_dim]
+ *      key, value   [num_tokens][num_kv_heads][head_dim], token stride given
+ *      slot_mapping int64 [num_tokens]
+ *  - q-head h reads kv-head h / (num_heads / num_kv_heads) (MHA, GQA, MQA).
+ *  - Supported: block_size 16; head_dim 64 or 128; pa_dtype F32 or BF16 for
+ *    q, key/value, pools and out alike (fp32 accumulation in every case).
+ *    Anything else returns PA_ERR_UNSUPPORTED.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+    PA_ERR_UNSUPPORTED = 2,  /* a valid shape this build does not implement */
+    PA_ERR_OUT_OF_RANGE = 3, /* data-dependent index error (device status) */
+    PA_ERR_WORKSPACE = 4,    /* workspace missing or too small */
+    PA_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+    PA_ERR_TIMEOUT = 6       /* a bounded in-kernel wait ran out (device status) */
+} pa_status;
+
+typedef enum { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1 } pa_dtype;
+
+/* Human-readable name of a status code.  Never NULL. */
+PA_API const char *pa_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+PA_API int pa_version(void);
+
+/*
+ * Number of blocks that hold num_tokens tokens: ceil(num_tokens / block_size)
+ * ([iitog] allocate_slots: 17 new tokens at block size 16 need 2 blocks).
+ * Host-only.  Returns -1 when num_tokens < 0 or block_size <= 0.
+ */
+PA_API int pa_num_blocks_needed(int num_tokens, int block_size);
+
+/*
+ * Slot mapping ([iitog] model runner builds the slot map; [kwkr] §1.2-1.3):
+ * for new token j of sequence s (cu_seqlens_q[s] <= j < cu_seqlens_q[s+1]),
+ * at logical position p = seq_start[s] + (j - cu_seqlens_q[s]),
+ *     slot_mapping[j] = block_tables[s][p / block_size] * block_size
+ *                       + p % block_size.
+ *  block_tables  device int32 [num_seqs][max_blocks]
+ *  seq_start     device int32 [num_seqs]: tokens already cached before the step
+ *  cu_seqlens_q  device int32 [num_seqs + 1], cu_seqlens_q[0] = 0,
+ *                cu_seqlens_q[num_seqs] = total_new
+ *  slot_mapping  device int64 [total_new] (output)
+ * A token whose logical block is >= max_blocks or whose table entry lies
+ * outside [0, num_blocks) gets slot -1 and sets PA_ERR_OUT_OF_RANGE.
+ */
+PA_API pa_status pa_compute_slot_mapping(const int32_t *block_tables, int num_seqs, int max_blocks,
+                                  const int32_t *seq_start, const int32_t *cu_seqlens_q,
+                                  int total_new, int block_size, int num_blocks,
+                                  int64_t *slot_mapping, int32_t *dev_status,
+                                  pa_stream_t stream);
+
+/*
+ * KV-cache write ([kwkr] §1.3: store the new token's K/V vectors into its
+ * physical block):  for t < num_tokens with slot = slot_mapping[t] >= 0,
+ *     k_cache[slot / B][slot % B][:][:] = key[t][:][:]   (and v_cache / value).
+ * Rows are copied bit for bit.  A negative slot is skipped (padding).  A slot
+ * >= num_blocks * block_size is skipped and sets PA_ERR_OUT_OF_RANGE.
+ *  key, value      device [num_tokens][num_kv_heads][head_dim]; the token
+ *                  stride (in elements) may exceed num_kv_heads*head_dim so a
+ *                  fused QKV projection output can be passed directly
+ *  k_cache/v_cache device pools (see layouts above), written in place
+ * Precondition (not checked on the device): live slots are pairwise distinct
+ * and do not lie in a block that another sequence shares read-only.
+ */
+PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_stride_tok,
+                               int64_t value_stride_tok, void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                               int32_t *dev_status, pa_stream_t stream);
+
+/*
+ * Workspace bytes pa_decode needs for these sizes (0 is never returned).
+ * Independent of the data; depends only on the arguments.
+ */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks);
+
+/*
+ * Paged decode attention ([kwkr] §1.3 attention through the block table;
+ * [iitog] decode reads earlier tokens' KV from the cache): one query row per
+ * sequence, at position context_lens[s] - 1, for each q-head h with kv-head
+ * g = h / (num_heads / num_kv_heads):
+ *     x_j = scale * <q[s][h], K_s[j][g]>,  j < context_lens[s],
+ *     out[s][h] = sum_j softmax(x)_j V_s[j][g],
+ * where K_s[j] = k_cache[block_tables[s][j / B]][j % B] (same for V).
+ * context_lens counts the new token, which pa_reshape_and_cache has already
+ * written.  Long contexts are split across thread blocks and merged by a
+ * second kernel with the log-sum-exp rule
+ *     M = max m_i,  L = sum l_i e^{m_i - M},  o = sum e^{m_i - M} o_i / L.
+ *  out          device [num_seqs][num_heads][head_dim], dtype of q
+ *  q            device [num_seqs][num_heads][head_dim]
+ *  scale        the fp32 softmax scale, normally 1/sqrtf(head_dim)
+ *  workspace    device scratch of >= pa_decode_workspace_size(...) bytes,
+ *               16-byte aligned; its contents on entry do not matter
+ * Results are deterministic: they depend on context_lens and the device's SM
+ * count, never on which physical blocks hold the data.
+ */
+PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                    int num_heads, int num_kv_heads, int head_dim, int block_size,
+                    int max_blocks, int num_blocks, float scale, pa_dtype dtype,
+                    void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                    pa_stream_t stream);
+
+/* Workspace bytes pa_varlen_prefill needs for these sizes. */
+PA_API size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int max_blocks);
+
+/*
+ * Varlen paged prefill over one concatenated super-sequence ([iitog] model
+ * runner: all sequences concatenated, masks and positions keep each on its
+ * own tokens; chunked prefill over a cached prefix).  Sequence s owns query
+ * rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1; with q_len = that count and
+ * ctx = context_lens[s] (cached prefix plus the new tokens, already written
+ * to the pools), query row i sits at position ctx - q_len + i and attends
+ * causally to keys 0 .. ctx - q_len + i of its own sequence only:
+ *     out[row][h] = sum_{j <= pos} softmax_j(scale * <q[row][h], K_s[j][g]>) V_s[j][g].
+ * Sequences with q_len == 1 (decode rows of a mixed step) take the decode
+ * kernels; the others take the prefill kernel.  q_len == 0 is allowed and
+ * produces nothing.  max_q_len bounds every q_len (a larger one sets
+ * PA_ERR_OUT_OF_RANGE and its rows are unspecified).
+ *  out, q       device [total_q][num_heads][head_dim]
+ *  cu_seqlens_q device int32 [num_seqs + 1]
+ *  workspace    >= pa_varlen_prefill_workspace_size(...) bytes, 16-byte aligned
+ */
+PA_API pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_q,
+                            const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens,
+                            int num_seqs, int total_q, int max_q_len, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                            int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream);
+
+/*
+ * Copies the device status word to *host_out after synchronising `stream`.
+ * Returns PA_ERR_CUDA if the copy fails (for example after a sticky fault).
+ */
+PA_API pa_status pa_get_device_status(const int32_t *dev_status, int32_t *host_out, pa_stream_t stream);
+
+/* Sets the device status word to PA_OK (asynchronous on `stream`). */
+PA_API pa_status pa_reset_device_status(int32_t *dev_status, pa_stream_t stream);
+
+/*
+ * Optional timing hook for profiling (no counterpart on the pages).  When
+ * both are non-NULL, ev_begin and ev_end (cudaEvent_t handles created by the
+ * caller) are recorded on the call's stream immediately before and after the
+ * main attention kernel of every later pa_decode / pa_varlen_prefill call made
+ * from the same host thread, so that kernel can be timed on its own.  Pass
+ * NULL, NULL to stop.  The events are not owned by the library.
+ */
+PA_API pa_status pa_set_timing_events(void *ev_begin, void *ev_end);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

@@ -1,0 +1,665 @@
+// attn_decode.cu -- persistent split-KV paged decode for bf16 caches.
+//
+// What it computes ("vLLM：颠覆大模型推理的高效API服务引擎深度解析" §1.3:
+// attention gathers the scattered physical blocks through the block table;
+// "vLLM изнутри…", model-runner paragraph: decode reads earlier tokens' KV
+// from the cache and is memory-bound): for every sequence s and q-head h,
+//     out[s][h] = sum_j softmax_j(scale * <q[s][h], K_s[j][g(h)]>) V_s[j][g(h)].
+//
+// How (the design is this library's own, built around HBM streaming):
+//  * plan kernel -- from context_lens, an exclusive prefix over the number of
+//    16-token blocks each sequence needs, and one 16-byte entry per logical
+//    block of the whole batch (sequence, query row, physical block id, valid
+//    tokens).  The batch becomes one stream of T blocks; with NHG kv-head
+//    groups the virtual stream has NHG*T entries.
+//  * main kernel -- one persistent CTA per SM takes an equal contiguous slice
+//    of the virtual stream, so every CTA reads the same number of cache bytes
+//    whatever the length mix.  A producer warp loads each 16-token block of
+//    KVH kv-heads (32 KB of K and 32 KB of V for 8 heads x 128 dims) with one
+//    TMA tensor copy each into a ring of shared-memory stages (128-byte
+//    swizzle), plus the sequence's query heads when a new sequence starts.
+//    Consumer warp kh owns kv-head kh and its G query heads: S = Q K^T and
+//    O += P V run on the tensor cores (mma m16n8k16, bf16 in, fp32 out),
+//    with an online softmax (running max / sum, base-2 exponent) in fp32.
+//    A sequence slice wholly inside one CTA is normalised and stored; a
+//    sequence cut by CTA boundaries leaves (m, l, o) partials.
+//  * reduce kernel -- merges the partials of cut sequences:
+//        M = max m_i, L = sum l_i 2^{m_i - M}, o = sum 2^{m_i - M} o_i / L.
+// Every cache byte is read once from HBM; the partition depends only on
+// context_lens and the CTA count, so results are bitwise reproducible and do
+// not depend on which physical blocks hold the data.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kB = kBlockSize;  // 16 tokens per block
+constexpr int kMaxKvhPerCta = 8;
+constexpr int kMaxQHeadsPerCta = 32;
+constexpr int kMaxGroup = 16;       // one m16 tile of query heads per kv-head
+constexpr int kMaxSeqs = 16384;     // prefix of all sequences kept in shared memory
+constexpr int kPartialCtas = 512;   // partial slots reserved for CTA boundaries
+constexpr int kPlanThreads = 256;
+constexpr int kSmemBudget = 227 * 1024;
+
+struct __align__(16) StreamEntry {
+    int32_t seq;
+    int32_t qrow;    // query / output row of the sequence
+    int32_t blk;     // physical block id, -1 if the table entry was invalid
+    int32_t packed;  // ntok (bits 0..5) | last block of its sequence (bit 6) | logical block << 8
+};
+
+struct __align__(16) StageHeader {
+    int32_t seq, qrow, hg, lb, ntok, flags, pad0, pad1;
+};
+constexpr int kFirst = 1, kLast = 2, kSeqEnd = 4, kValid = 8;
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    const int32_t *prefix;     // [num_seqs + 1]
+    const StreamEntry *stream; // [T]
+    float *part_o;             // [slots][QH][D]
+    float *part_ml;            // [slots][QH][2]
+    int num_seqs;
+    int num_heads;
+    int kvh;       // kv-heads per CTA
+    int group;     // q-heads per kv-head
+    int qh;        // q-heads per CTA = kvh * group
+    int nhg;       // kv-head groups
+    int num_stages;
+    int tma_heads; // kv-heads per TMA op (kvh, or 1 with the per-head map)
+    float scale_log2;
+    int32_t *status;
+};
+
+// ------------------------------------------------------------------ plan
+__global__ void __launch_bounds__(kPlanThreads)
+    decode_plan_kernel(const int32_t *__restrict__ context_lens,
+                       const int32_t *__restrict__ cu_seqlens_q,
+                       const int32_t *__restrict__ block_tables, int num_seqs, int max_blocks,
+                       int num_blocks, int total_q, int32_t *__restrict__ prefix,
+                       StreamEntry *__restrict__ stream, int32_t *status) {
+    extern __shared__ int32_t pref_s[];  // [num_seqs + 1]
+    __shared__ int32_t warp_tot[kPlanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int running = 0;
+    for (int base = 0; base < num_seqs; base += kPlanThreads) {
+        const int s = base + tid;
+        int nb = 0;
+        if (s < num_seqs) {
+            const int q0 = cu_seqlens_q ? __ldg(cu_seqlens_q + s) : s;
+            const int q1 = cu_seqlens_q ? __ldg(cu_seqlens_q + s + 1) : s + 1;
+            const int q_len = q1 - q0;
+            const int ctx = __ldg(context_lens + s);
+            if (q0 < 0 || q1 < q0 || q1 > total_q) {
+                if (blockIdx.x == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
+            } else if (q_len == 1) {
+                if (ctx <= 0 || (int64_t)ctx > (int64_t)max_blocks * kB) {
+                    if (blockIdx.x == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
+                } else {
+                    nb = (ctx + kB - 1) / kB;
+                }
+            }
+        }
+        int incl = nb;  // inclusive warp scan
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int warp_off = 0, chunk_tot = 0;
+        for (int w = 0; w < kPlanThreads / 32; ++w) {
+            const int t = warp_tot[w];
+            if (w < warp) warp_off += t;
+            chunk_tot += t;
+        }
+        if (s < num_seqs) pref_s[s] = running + warp_off + incl - nb;
+        running += chunk_tot;
+        __syncthreads();
+    }
+    if (tid == 0) pref_s[num_seqs] = running;
+    __syncthreads();
+    const int T = running;
+    if (blockIdx.x == 0)
+        for (int s = tid; s <= num_seqs; s += kPlanThreads) prefix[s] = pref_s[s];
+    for (int b = blockIdx.x * kPlanThreads + tid; b < T; b += gridDim.x * kPlanThreads) {
+        int lo = 0, hi = num_seqs;  // last s with pref_s[s] <= b
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pref_s[mid] <= b) lo = mid; else hi = mid;
+        }
+        const int s = lo;
+        const int lb = b - pref_s[s];
+        const int ctx = __ldg(context_lens + s);
+        int32_t blk = __ldg(block_tables + (int64_t)s * max_blocks + lb);
+        if (blk < 0 || blk >= num_blocks) {
+            set_status(status, PA_ERR_OUT_OF_RANGE);
+            blk = -1;
+        }
+        const int ntok = min(kB, ctx - lb * kB);
+        const int seq_end = (lb + 1) * kB >= ctx ? 1 : 0;
+        StreamEntry e;
+        e.seq = s;
+        e.qrow = cu_seqlens_q ? __ldg(cu_seqlens_q + s) : s;
+        e.blk = blk;
+        e.packed = ntok | (seq_end << 6) | (lb << 8);
+        stream[b] = e;
+    }
+}
+
+__device__ __forceinline__ int64_t cta_slice_begin(int64_t c, int64_t nv, int64_t p) {
+    return c * nv / p;
+}
+// CTA whose slice holds virtual block v.
+__device__ __forceinline__ int64_t cta_of(int64_t v, int64_t nv, int64_t p) {
+    return ((v + 1) * p - 1) / nv;
+}
+
+// ------------------------------------------------------------------ main kernel
+template <int D>
+__global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
+    split_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+    constexpr int kHeadTileBytes = kB * D * 2;    // one kv-head of one block
+    constexpr int kKSteps = D / 16;
+    constexpr int kNTiles = D / 8;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const int kvh = p.kvh, NS = p.num_stages;
+    const int kv_tile = kvh * kHeadTileBytes;
+    const int q_tile = p.qh * D * 2;
+    const int stage_bytes = (2 * kv_tile + q_tile + 1023) & ~1023;
+    StageHeader *hdr = reinterpret_cast<StageHeader *>(smem + NS * stage_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(hdr + NS);
+    uint64_t *empty = full + NS;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, kvh);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+
+    const int S = p.num_seqs;
+    const int64_t T = __ldg(p.prefix + S);
+    const int64_t NV = T * p.nhg;
+    const int64_t P = gridDim.x;
+    const int64_t lo = cta_slice_begin(blockIdx.x, NV, P);
+    const int64_t hi = cta_slice_begin(blockIdx.x + 1, NV, P);
+    const int nloc = (int)(hi - lo);
+    if (nloc <= 0) return;
+
+    if (warp == kvh) {
+        // ================= producer warp
+        if (lane == 0) {
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
+        auto load_entry = [&](int64_t v, StreamEntry &e, int &hg) {
+            if (v < hi) {
+                hg = (int)(v / T);
+                e = p.stream[v - (int64_t)hg * T];
+            } else {
+                hg = -1;
+                e.seq = -1; e.qrow = 0; e.blk = -1; e.packed = 0;
+            }
+        };
+        StreamEntry cur, nxt;
+        int cur_hg, nxt_hg;
+        load_entry(lo + lane, cur, cur_hg);
+        int prev_seq = -1, prev_hg = -1;
+        int issued = 0;
+        bool ok = true;
+        for (int64_t base = lo; base < hi && ok; base += 32) {
+            load_entry(base + 32 + lane, nxt, nxt_hg);  // prefetch the next chunk
+            const int n = (int)(hi - base < 32 ? hi - base : 32);
+            const int next_seq_first = __shfl_sync(0xffffffffu, nxt.seq, 0);
+            const int next_hg_first = __shfl_sync(0xffffffffu, nxt_hg, 0);
+            for (int i = 0; i < n; ++i) {
+                const int seq = __shfl_sync(0xffffffffu, cur.seq, i);
+                const int qrow = __shfl_sync(0xffffffffu, cur.qrow, i);
+                const int blk = __shfl_sync(0xffffffffu, cur.blk, i);
+                const int packed = __shfl_sync(0xffffffffu, cur.packed, i);
+                const int hg = __shfl_sync(0xffffffffu, cur_hg, i);
+                const int nseq = i + 1 < 32 ? __shfl_sync(0xffffffffu, cur.seq, (i + 1) & 31) : next_seq_first;
+                const int nhg = i + 1 < 32 ? __shfl_sync(0xffffffffu, cur_hg, (i + 1) & 31) : next_hg_first;
+                if (lane == 0) {
+                    const int k = issued;
+                    const int stage = k % NS;
+                    if (k >= NS && !mbar_wait(empty + stage, ((k / NS) - 1) & 1)) {
+                        set_status(p.status, PA_ERR_TIMEOUT);
+                        abort_flag = 1;
+                        ok = false;
+                    }
+                    if (ok) {
+                        const bool first = (seq != prev_seq) || (hg != prev_hg);
+                        const bool last = (base + i + 1 == hi) || (nseq != seq) || (nhg != hg);
+                        StageHeader h;
+                        h.seq = seq;
+                        h.qrow = qrow;
+                        h.hg = hg;
+                        h.lb = packed >> 8;
+                        h.ntok = packed & 63;
+                        h.flags = (first ? kFirst : 0) | (last ? kLast : 0) |
+                                  ((packed >> 6) & 1 ? kSeqEnd : 0) | (blk >= 0 ? kValid : 0);
+                        h.pad0 = h.pad1 = 0;
+                        hdr[stage] = h;
+                        uint8_t *st = smem + (size_t)stage * stage_bytes;
+                        const uint32_t bytes = (blk >= 0 ? 2u * kv_tile : 0u) + (first ? (uint32_t)q_tile : 0u);
+                        if (bytes) mbar_arrive_expect_tx(full + stage, bytes);
+                        else mbar_arrive(full + stage);
+                        if (blk >= 0) {
+                            const int h0 = hg * kvh;
+                            for (int t = 0; t < kvh; t += p.tma_heads) {
+                                tma_load_5d(st + t * kHeadTileBytes, &tmap_k, 0, 0, 0, h0 + t, blk, full + stage);
+                                tma_load_5d(st + kv_tile + t * kHeadTileBytes, &tmap_v, 0, 0, 0, h0 + t, blk,
+                                            full + stage);
+                            }
+                        }
+                        if (first) {
+                            const __nv_bfloat16 *qsrc =
+                                p.q + ((int64_t)qrow * p.num_heads + (int64_t)hg * p.qh) * D;
+                            bulk_g2s(st + 2 * kv_tile, qsrc, q_tile, full + stage);
+                        }
+                        prev_seq = seq;
+                        prev_hg = hg;
+                        ++issued;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+            }
+            cur = nxt;
+            cur_hg = nxt_hg;
+        }
+        // wait (bounded) until every copy this CTA issued has landed
+        if (lane == 0) {
+            const int first_k = issued > NS ? issued - NS : 0;
+            for (int k = first_k; k < issued; ++k) mbar_wait(full + (k % NS), (k / NS) & 1);
+        }
+        return;
+    }
+
+    // ================= consumer warp kh: kv-head kh of the CTA's group
+    const int kh = warp;
+    const int G = p.group;
+    const int r = lane >> 2;        // query head row inside the m16 tile
+    const int quad = lane & 3;
+    const bool row_ok = r < G;
+    // ldmatrix lane addressing inside one kv-head tile (128-byte rows, swizzled)
+    const int mi = lane >> 3, rr = lane & 7;
+    const int k_tok = ((mi >> 1) << 3) + rr, k_dsub = mi & 1;
+    const int v_tok = ((mi & 1) << 3) + rr, v_dsub = mi >> 1;
+
+    float o[kNTiles][4];
+    uint32_t qa[kKSteps][2];
+    float m_run = -INFINITY, l_run = 0.f;
+    int piece_lb0 = 0;
+
+    for (int k = 0; k < nloc; ++k) {
+        const int stage = k % NS;
+        if (*reinterpret_cast<volatile int *>(&abort_flag)) break;
+        if (!mbar_wait(full + stage, (k / NS) & 1)) {
+            if (lane == 0) set_status(p.status, PA_ERR_TIMEOUT);
+            abort_flag = 1;
+            break;
+        }
+        const StageHeader h = hdr[stage];
+        const uint8_t *st = smem + (size_t)stage * stage_bytes;
+        if (h.flags & kFirst) {
+            const uint8_t *qs = st + 2 * kv_tile + (size_t)(kh * G + r) * D * 2;
+#pragma unroll
+            for (int ks = 0; ks < kKSteps; ++ks) {
+                qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + quad * 2) * 2) : 0u;
+                qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + 8 + quad * 2) * 2) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < kNTiles; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+            m_run = -INFINITY;
+            l_run = 0.f;
+            piece_lb0 = h.lb;
+        }
+        if (h.flags & kValid) {
+            const uint32_t kbase = smem_u32(st + kh * kHeadTileBytes);
+            const uint32_t vbase = smem_u32(st + kv_tile + kh * kHeadTileBytes);
+            // ---- S = Q K^T : two n-tiles of 8 tokens
+            float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < kKSteps; ++ks) {
+                const int chunk = ((ks & 3) << 1) + k_dsub;
+                const uint32_t addr = kbase + (ks >> 2) * (kB * 128) + k_tok * 128 +
+                                      ((chunk ^ (k_tok & 7)) << 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(addr, b0, b1, b2, b3);
+                mma_bf16_16816(sacc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+                mma_bf16_16816(sacc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+            }
+            // ---- online softmax on row r (tokens 2q, 2q+1, 8+2q, 9+2q)
+            const int ntok = h.ntok;
+            float x[2][2];
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = nt * 8 + quad * 2 + e;
+                    const float val = tok < ntok ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+                    x[nt][e] = val;
+                    tmax = fmaxf(tmax, val);
+                }
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+            const float m_new = fmaxf(m_run, tmax);
+            if (m_new != -INFINITY) {
+                const float alpha = fast_exp2(m_run - m_new);
+                float pr[2][2];
+                float psum = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        pr[nt][e] = fast_exp2(x[nt][e] - m_new);
+                        psum += pr[nt][e];
+                    }
+                l_run = l_run * alpha + psum;
+                m_run = m_new;
+#pragma unroll
+                for (int j = 0; j < kNTiles; ++j) {
+                    o[j][0] *= alpha;
+                    o[j][1] *= alpha;
+                }
+                const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
+                const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
+                // masks for value rows past the sequence end (they may hold anything)
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (ntok < kB) {
+                    const int t0 = quad * 2;
+                    mlo = (t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u);
+                    mhi = (t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u);
+                }
+                // ---- O += P V : D/8 n-tiles of 8 dims, k = 16 tokens
+#pragma unroll
+                for (int j2 = 0; j2 < kNTiles / 2; ++j2) {
+                    const int chunk = ((j2 & 3) << 1) + v_dsub;
+                    const uint32_t addr = vbase + (j2 >> 2) * (kB * 128) + v_tok * 128 +
+                                          ((chunk ^ (v_tok & 7)) << 4);
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(addr, v0, v1, v2, v3);
+                    v0 &= mlo; v2 &= mlo; v1 &= mhi; v3 &= mhi;
+                    mma_bf16_16816(o[2 * j2], pa0, 0u, pa2, 0u, v0, v1);
+                    mma_bf16_16816(o[2 * j2 + 1], pa0, 0u, pa2, 0u, v2, v3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + stage);
+
+        if (h.flags & kLast) {
+            float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+            l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+            const bool whole = piece_lb0 == 0 && (h.flags & kSeqEnd);
+            const int h_loc = kh * G + r;
+            if (row_ok) {
+                if (whole) {
+                    const float inv = 1.f / l_row;
+                    __nv_bfloat16 *dst = p.out + ((int64_t)h.qrow * p.num_heads +
+                                                  (int64_t)h.hg * p.qh + h_loc) * D + quad * 2;
+#pragma unroll
+                    for (int j = 0; j < kNTiles; ++j)
+                        *reinterpret_cast<uint32_t *>(dst + j * 8) =
+                            pack_bf16x2(o[j][0] * inv, o[j][1] * inv);
+                } else {
+                    const int64_t slot = (int64_t)h.hg * S + h.seq + blockIdx.x;
+                    float *dst = p.part_o + (slot * p.qh + h_loc) * D + quad * 2;
+#pragma unroll
+                    for (int j = 0; j < kNTiles; ++j)
+                        *reinterpret_cast<float2 *>(dst + j * 8) = make_float2(o[j][0], o[j][1]);
+                    if (quad == 0)
+                        *reinterpret_cast<float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2) =
+                            make_float2(m_run, l_row);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ reduce
+template <int D>
+__global__ void __launch_bounds__(256)
+    split_decode_reduce_kernel(const DecodeParams p, int num_ctas) {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.num_seqs;
+    const int vs = gw / p.qh, h_loc = gw % p.qh;
+    if (vs >= p.nhg * S) return;
+    const int hg = vs / S, s = vs % S;
+    const int64_t T = __ldg(p.prefix + S);
+    const int64_t NV = T * p.nhg;
+    const int64_t b0 = __ldg(p.prefix + s), b1 = __ldg(p.prefix + s + 1);
+    if (b1 == b0) return;
+    const int64_t c0 = cta_of(hg * T + b0, NV, num_ctas);
+    const int64_t c1 = cta_of(hg * T + b1 - 1, NV, num_ctas);
+    if (c0 == c1) return;  // whole sequence inside one CTA: already written
+    float M = -INFINITY;
+    for (int64_t c = c0; c <= c1; ++c) M = fmaxf(M, p.part_ml[((vs + c) * p.qh + h_loc) * 2]);
+    constexpr int kPer = D / 32;
+    float acc[kPer];
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) acc[t] = 0.f;
+    float L = 0.f;
+    for (int64_t c = c0; c <= c1; ++c) {
+        const int64_t slot = vs + c;
+        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2);
+        const float w = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+        L += ml.y * w;
+        const float *src = p.part_o + (slot * p.qh + h_loc) * D;
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) acc[t] = fmaf(w, src[lane + 32 * t], acc[t]);
+    }
+    const int qrow = __ldg(&p.stream[b0].qrow);
+    __nv_bfloat16 *dst = p.out + ((int64_t)qrow * p.num_heads + (int64_t)hg * p.qh + h_loc) * D;
+    const float inv = 1.f / L;
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) dst[lane + 32 * t] = __float2bfloat16_rn(acc[t] * inv);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Pool [num_blocks][16][Hkv][D] bf16 seen as a 5-D tensor whose box is one
+// block for `box_heads` kv-heads, laid out in shared memory as
+// [head][D/64][token][64] with 128-byte rows and the 128-byte swizzle.
+CUresult make_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int D,
+                       int box_heads, bool permuted) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t eb = 2;
+    cuuint64_t dims[5];
+    cuuint64_t strides[4];
+    cuuint32_t box[5];
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (permuted) {
+        // dims: d_lo(64), token(16), d_hi(D/64), head(Hkv), block
+        dims[0] = 64; dims[1] = kB; dims[2] = D / 64; dims[3] = hkv; dims[4] = num_blocks;
+        strides[0] = (cuuint64_t)hkv * D * eb;   // token
+        strides[1] = 64 * eb;                     // d_hi
+        strides[2] = (cuuint64_t)D * eb;          // head
+        strides[3] = (cuuint64_t)kB * hkv * D * eb;  // block
+        box[0] = 64; box[1] = kB; box[2] = D / 64; box[3] = box_heads; box[4] = 1;
+    } else {
+        return CUDA_ERROR_INVALID_VALUE;
+    }
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+struct Layout {
+    int kvh, group, qh, nhg;
+};
+
+Layout decode_layout(int num_heads, int num_kv_heads) {
+    Layout L;
+    L.group = num_heads / num_kv_heads;
+    int kvh = num_kv_heads < kMaxKvhPerCta ? num_kv_heads : kMaxKvhPerCta;
+    while (kvh > 1 && (kvh * L.group > kMaxQHeadsPerCta || num_kv_heads % kvh != 0)) --kvh;
+    L.kvh = kvh;
+    L.qh = kvh * L.group;
+    L.nhg = num_kv_heads / kvh;
+    return L;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WorkspaceLayout {
+    size_t prefix, stream, part_ml, part_o, total;
+};
+
+WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_blocks) {
+    WorkspaceLayout w;
+    const size_t slots_heads = ((size_t)num_seqs + kPartialCtas) * num_heads;
+    w.prefix = 0;
+    w.stream = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 256);
+    w.part_ml = align_up(w.stream + sizeof(StreamEntry) * (size_t)num_seqs * max_blocks, 256);
+    w.part_o = align_up(w.part_ml + sizeof(float) * 2 * slots_heads, 256);
+    w.total = align_up(w.part_o + sizeof(float) * (size_t)head_dim * slots_heads, 256);
+    return w;
+}
+
+template <int D>
+cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtensorMap &mk,
+                        const CUtensorMap &mv, int grid, cudaStream_t stream) {
+    const int kv_tile = prm.kvh * kB * D * 2;
+    const int stage_bytes = (int)align_up(2 * kv_tile + prm.qh * D * 2, 1024);
+    const size_t smem = 1024 + (size_t)prm.num_stages * (stage_bytes + sizeof(StageHeader) + 16);
+    auto kern = split_decode_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    timing_begin(stream);
+    kern<<<grid, 32 * (prm.kvh + 1), smem, stream>>>(mk, mv, prm);
+    timing_end(stream);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int warps = prm.nhg * prm.num_seqs * prm.qh;
+    split_decode_reduce_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(prm, grid);
+    return cudaGetLastError();
+}
+
+int stages_for(int kvh, int qh, int D) {
+    const int kv_tile = kvh * kB * D * 2;
+    const int stage_bytes = (int)align_up(2 * kv_tile + qh * D * 2, 1024);
+    int ns = (kSmemBudget - 1024) / (stage_bytes + (int)sizeof(StageHeader) + 16);
+    return ns > 8 ? 8 : ns;
+}
+
+}  // namespace
+
+bool split_decode_supported(const AttnArgs &a) {
+    if (a.dtype != PA_DTYPE_BF16 || a.block_size != kB) return false;
+    if (a.head_dim != 64 && a.head_dim != 128) return false;
+    if (a.num_seqs > kMaxSeqs) return false;
+    if ((int64_t)a.num_seqs * a.max_blocks >= (int64_t)1 << 30) return false;
+    const int G = a.num_heads / a.num_kv_heads;
+    if (G > kMaxGroup) return false;
+    const Layout L = decode_layout(a.num_heads, a.num_kv_heads);
+    if (L.qh > kMaxQHeadsPerCta) return false;
+    if (stages_for(L.kvh, L.qh, a.head_dim) < 2) return false;
+    auto al = [](const void *ptr, uintptr_t n) { return reinterpret_cast<uintptr_t>(ptr) % n == 0; };
+    return al(a.q, 16) && al(a.k_cache, 16) && al(a.v_cache, 16) && al(a.out, 4);
+}
+
+size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max_blocks) {
+    return workspace_layout(num_seqs, num_heads, head_dim, max_blocks).total;
+}
+
+cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+    if (a.num_seqs == 0) return cudaSuccess;
+    const WorkspaceLayout w = workspace_layout(a.num_seqs, a.num_heads, a.head_dim, a.max_blocks);
+    if (workspace_bytes < w.total) return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const Layout L = decode_layout(a.num_heads, a.num_kv_heads);
+
+    DecodeParams prm;
+    prm.q = static_cast<const __nv_bfloat16 *>(a.q);
+    prm.out = static_cast<__nv_bfloat16 *>(a.out);
+    prm.prefix = reinterpret_cast<const int32_t *>(ws + w.prefix);
+    prm.stream = reinterpret_cast<const StreamEntry *>(ws + w.stream);
+    prm.part_ml = reinterpret_cast<float *>(ws + w.part_ml);
+    prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    prm.num_seqs = a.num_seqs;
+    prm.num_heads = a.num_heads;
+    prm.kvh = L.kvh;
+    prm.group = L.group;
+    prm.qh = L.qh;
+    prm.nhg = L.nhg;
+    prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim);
+    prm.scale_log2 = a.scale * 1.4426950408889634f;
+    prm.status = a.status;
+
+    // tensor maps: one TMA per block for all kv-heads of the CTA
+    CUtensorMap mk, mv;
+    prm.tma_heads = L.kvh;
+    if (make_pool_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, L.kvh, true) != CUDA_SUCCESS ||
+        make_pool_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, L.kvh, true) != CUDA_SUCCESS) {
+        // one TMA per kv-head
+        prm.tma_heads = 1;
+        if (make_pool_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1, true) != CUDA_SUCCESS ||
+            make_pool_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1, true) != CUDA_SUCCESS)
+            return cudaErrorNotSupported;
+    }
+
+    // plan
+    const size_t plan_smem = sizeof(int32_t) * ((size_t)a.num_seqs + 1);
+    cudaError_t e = cudaFuncSetAttribute(decode_plan_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
+    if (e != cudaSuccess) return e;
+    const int64_t max_entries = (int64_t)a.num_seqs * a.max_blocks;
+    const int sms = device_sm_count();
+    int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
+    if (plan_grid > 2 * sms) plan_grid = 2 * sms;
+    if (plan_grid < 1) plan_grid = 1;
+    decode_plan_kernel<<<plan_grid, kPlanThreads, plan_smem, stream>>>(
+        a.context_lens, a.cu_seqlens_q, a.block_tables, a.num_seqs, a.max_blocks, a.num_blocks,
+        a.total_q, reinterpret_cast<int32_t *>(ws + w.prefix), reinterpret_cast<StreamEntry *>(ws + w.stream),
+        a.status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    int grid = sms;
+    if (grid > kPartialCtas) grid = kPartialCtas;
+    return a.head_dim == 64 ? launch_main<64>(a, prm, mk, mv, grid, stream)
+                            : launch_main<128>(a, prm, mk, mv, grid, stream);
+}
+
+}  // namespace pa

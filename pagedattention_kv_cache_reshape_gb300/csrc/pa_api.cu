@@ -1,0 +1,240 @@
+// pa_api.cu -- the extern "C" entry points declared in include/pa.h: host-side
+// argument validation, workspace sizing and dispatch to the kernels.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+int device_sm_count() {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+namespace {
+thread_local cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+}  // namespace
+
+void timing_begin(cudaStream_t stream) {
+    if (g_ev_begin && g_ev_end) cudaEventRecord(g_ev_begin, stream);
+}
+void timing_end(cudaStream_t stream) {
+    if (g_ev_begin && g_ev_end) cudaEventRecord(g_ev_end, stream);
+}
+
+namespace {
+
+pa_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return PA_OK;
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    return PA_ERR_CUDA;
+}
+
+int elem_bytes(pa_dtype d) {
+    return d == PA_DTYPE_F32 ? 4 : (d == PA_DTYPE_BF16 ? 2 : 0);
+}
+
+bool aligned(const void *p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// Shape checks shared by the attention calls.
+pa_status check_attention_shape(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks, int num_blocks, pa_dtype dtype,
+                                float scale) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN
+    if (elem_bytes(dtype) == 0) return PA_ERR_INVALID_ARG;
+    if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 32) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks * block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char *pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int pa_version(void) { return 100; }
+
+int pa_num_blocks_needed(int num_tokens, int block_size) {
+    if (num_tokens < 0 || block_size <= 0) return -1;
+    return num_tokens / block_size + (num_tokens % block_size != 0 ? 1 : 0);
+}
+
+pa_status pa_compute_slot_mapping(const int32_t *block_tables, int num_seqs, int max_blocks,
+                                  const int32_t *seq_start, const int32_t *cu_seqlens_q,
+                                  int total_new, int block_size, int num_blocks,
+                                  int64_t *slot_mapping, int32_t *dev_status,
+                                  pa_stream_t stream) {
+    if (num_seqs < 0 || total_new < 0 || max_blocks <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (total_new > 0 && num_seqs == 0) return PA_ERR_INVALID_ARG;
+    if (total_new == 0) return PA_OK;
+    if (!block_tables || !seq_start || !cu_seqlens_q || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    return from_cuda(launch_slot_mapping(block_tables, num_seqs, max_blocks, seq_start,
+                                         cu_seqlens_q, total_new, block_size, num_blocks,
+                                         slot_mapping, dev_status, (cudaStream_t)stream));
+}
+
+pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_stride_tok,
+                               int64_t value_stride_tok, void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                               int32_t *dev_status, pa_stream_t stream) {
+    const int eb = elem_bytes(dtype);
+    if (eb == 0 || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (key_stride_tok < row || value_stride_tok < row) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned(key, eb) || !aligned(value, eb) || !aligned(k_cache, eb) || !aligned(v_cache, eb))
+        return PA_ERR_INVALID_ARG;
+    if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    return from_cuda(launch_reshape_and_cache(key, value, key_stride_tok, value_stride_tok,
+                                              k_cache, v_cache, slot_mapping, num_tokens,
+                                              num_kv_heads, head_dim, block_size, num_blocks, eb,
+                                              dev_status, (cudaStream_t)stream));
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks) {
+    (void)num_kv_heads;
+    (void)block_size;
+    if (num_seqs < 0) num_seqs = 0;
+    if (num_heads < 1) num_heads = 1;
+    if (head_dim < 1) head_dim = 1;
+    if (max_blocks < 1) max_blocks = 1;
+    return split_decode_workspace(num_seqs, num_heads, head_dim, max_blocks);
+}
+
+pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                    int num_heads, int num_kv_heads, int head_dim, int block_size,
+                    int max_blocks, int num_blocks, float scale, pa_dtype dtype,
+                    void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                    pa_stream_t stream) {
+    pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                         max_blocks, num_blocks, dtype, scale);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    const int eb = elem_bytes(dtype);
+    if (!aligned(out, eb) || !aligned(q, eb) || !aligned(k_cache, eb) || !aligned(v_cache, eb))
+        return PA_ERR_INVALID_ARG;
+    AttnArgs a{out, q, k_cache, v_cache, block_tables, context_lens, nullptr,
+               num_seqs, num_seqs, 1, num_heads, num_kv_heads, head_dim, block_size,
+               max_blocks, num_blocks, scale, dtype, dev_status};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (split_decode_supported(a)) {
+        const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                     block_size, max_blocks);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
+        return from_cuda(launch_split_decode(a, workspace, workspace_bytes, s));
+    }
+    return from_cuda(launch_generic_attention(a, false, s));
+}
+
+size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int max_blocks) {
+    (void)total_q;
+    return pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                    max_blocks);
+}
+
+pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_q,
+                            const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens,
+                            int num_seqs, int total_q, int max_q_len, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                            int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream) {
+    pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                         max_blocks, num_blocks, dtype, scale);
+    if (st != PA_OK) return st;
+    if (total_q < 0 || max_q_len < 0) return PA_ERR_INVALID_ARG;
+    if (total_q == 0 || num_seqs == 0) return PA_OK;
+    if (!out || !q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    const int eb = elem_bytes(dtype);
+    if (!aligned(out, eb) || !aligned(q, eb) || !aligned(k_cache, eb) || !aligned(v_cache, eb))
+        return PA_ERR_INVALID_ARG;
+    AttnArgs a{out, q, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q,
+               num_seqs, total_q, max_q_len, num_heads, num_kv_heads, head_dim, block_size,
+               max_blocks, num_blocks, scale, dtype, dev_status};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (split_decode_supported(a)) {
+        const size_t need = pa_varlen_prefill_workspace_size(num_seqs, total_q, num_heads,
+                                                             num_kv_heads, head_dim, block_size,
+                                                             max_blocks);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
+        // decode rows (q_len == 1) stream through the split-KV decode kernels,
+        // the prefill chunks through the attention kernel
+        cudaError_t e = launch_split_decode(a, workspace, workspace_bytes, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        if (max_q_len <= 1) return PA_OK;
+        return from_cuda(launch_generic_attention(a, true, s));
+    }
+    return from_cuda(launch_generic_attention(a, false, s));
+}
+
+pa_status pa_get_device_status(const int32_t *dev_status, int32_t *host_out, pa_stream_t stream) {
+    if (!dev_status || !host_out) return PA_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(host_out, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    return from_cuda(e);
+}
+
+pa_status pa_reset_device_status(int32_t *dev_status, pa_stream_t stream) {
+    if (!dev_status) return PA_ERR_INVALID_ARG;
+    return from_cuda(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), (cudaStream_t)stream));
+}
+
+pa_status pa_set_timing_events(void *ev_begin, void *ev_end) {
+    if ((ev_begin == nullptr) != (ev_end == nullptr)) return PA_ERR_INVALID_ARG;
+    g_ev_begin = static_cast<cudaEvent_t>(ev_begin);
+    g_ev_end = static_cast<cudaEvent_t>(ev_end);
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// pa_internal.h -- launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Paged-attention problem as seen by the launchers (all pointers on device).
+struct AttnArgs {
+    void *out;
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const int32_t *cu_seqlens_q;  // nullptr: one query row per sequence (decode)
+    int num_seqs;
+    int total_q;
+    int max_q_len;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    int max_blocks;
+    int num_blocks;
+    float scale;
+    pa_dtype dtype;
+    int32_t *status;
+};
+
+constexpr int kBlockSize = 16;     // tokens per cache block (the only one built)
+constexpr int kMaxPersistentCtas = 1024;
+
+int device_sm_count();  // SM count of the current device (cached per device)
+
+// Timing hook (pa_set_timing_events): records the caller's events, if set,
+// around the main attention kernel.
+void timing_begin(cudaStream_t stream);
+void timing_end(cudaStream_t stream);
+
+cudaError_t launch_slot_mapping(const int32_t *block_tables, int num_seqs, int max_blocks,
+                                const int32_t *seq_start, const int32_t *cu_seqlens_q,
+                                int total_new, int block_size, int num_blocks,
+                                int64_t *slot_mapping, int32_t *status, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t key_stride,
+                                     int64_t value_stride, void *k_cache, void *v_cache,
+                                     const int64_t *slot_mapping, int num_tokens,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     int num_blocks, int elem_bytes, int32_t *status,
+                                     cudaStream_t stream);
+
+// CUDA-core attention for every supported shape and dtype (one CTA per query
+// row and kv-head).  With skip_single_row, sequences whose q_len is 1 are left
+// to the decode kernels.
+cudaError_t launch_generic_attention(const AttnArgs &a, bool skip_single_row,
+                                     cudaStream_t stream);
+
+// Persistent TMA + tensor-core split-KV decode (bf16, head_dim 64/128).
+bool split_decode_supported(const AttnArgs &a);
+size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max_blocks);
+// With a.cu_seqlens_q set, only sequences with q_len == 1 are processed and
+// their query/output row is cu_seqlens_q[s].
+cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,247 @@
+"""Thin Python binding of the C ABI in include/pa.h (ctypes).
+
+Argument marshalling only: torch tensors supply device pointers, the current
+CUDA stream supplies the stream, and every step of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback: if ``libpa.so`` is missing
+or a call fails, an exception is raised.
+
+The functions keep the C names without the ``pa_`` prefix.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_RANGE, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+EXPORTS = (
+    "pa_status_string", "pa_version", "pa_num_blocks_needed", "pa_compute_slot_mapping",
+    "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
+    "pa_varlen_prefill_workspace_size", "pa_varlen_prefill", "pa_get_device_status",
+    "pa_reset_device_status", "pa_set_timing_events",
+)
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libpa.so (built by __graft_entry__.build() or build.py)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build the CUDA library first "
+                              "(python -m pagedattention_kv_cache_reshape_gb300.build)")
+        L = ctypes.CDLL(path)
+        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_status_string.argtypes = [i32]
+        L.pa_version.restype = i32
+        L.pa_num_blocks_needed.restype = i32
+        L.pa_num_blocks_needed.argtypes = [i32, i32]
+        L.pa_compute_slot_mapping.restype = i32
+        L.pa_compute_slot_mapping.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, vp, vp, vp]
+        L.pa_reshape_and_cache.restype = i32
+        L.pa_reshape_and_cache.argtypes = [vp, vp, i64, i64, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        L.pa_decode_workspace_size.restype = sz
+        L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.pa_decode.restype = i32
+        L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                vp, sz, vp, vp]
+        L.pa_varlen_prefill_workspace_size.restype = sz
+        L.pa_varlen_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        L.pa_varlen_prefill.restype = i32
+        L.pa_varlen_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, i32, f32, i32, vp, sz, vp, vp]
+        L.pa_get_device_status.restype = i32
+        L.pa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+        L.pa_reset_device_status.restype = i32
+        L.pa_reset_device_status.argtypes = [vp, vp]
+        L.pa_set_timing_events.restype = i32
+        L.pa_set_timing_events.argtypes = [vp, vp]
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != OK:
+        raise PAError(rc, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _contig(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return _dev(t, name, dtype)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _opt(t) -> int:
+    return 0 if t is None else _dev(t, "dev_status", torch.int32)
+
+
+# ------------------------------------------------------------------ calls
+
+def version() -> int:
+    return int(load().pa_version())
+
+
+def num_blocks_needed(num_tokens: int, block_size: int) -> int:
+    return int(load().pa_num_blocks_needed(int(num_tokens), int(block_size)))
+
+
+def compute_slot_mapping(block_tables, seq_start, cu_seqlens_q, num_blocks: int, total_new: int,
+                         block_size: int = 16, slot_mapping=None, dev_status=None, stream=None):
+    """pa_compute_slot_mapping; returns the int64 slot_mapping tensor."""
+    num_seqs, max_blocks = block_tables.shape
+    if slot_mapping is None:
+        slot_mapping = torch.empty(total_new, dtype=torch.int64, device=block_tables.device)
+    rc = load().pa_compute_slot_mapping(
+        _contig(block_tables, "block_tables", torch.int32), num_seqs, max_blocks,
+        _contig(seq_start, "seq_start", torch.int32), _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32),
+        int(total_new), int(block_size), int(num_blocks),
+        _contig(slot_mapping, "slot_mapping", torch.int64), _opt(dev_status), _stream(stream))
+    _check(rc, "pa_compute_slot_mapping")
+    return slot_mapping
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, dev_status=None, stream=None):
+    """pa_reshape_and_cache; key/value may be token-strided views (rows contiguous)."""
+    num_blocks, block_size, hkv, d = k_cache.shape
+    for name, t in (("key", key), ("value", value)):
+        if t.dim() != 3 or t.shape[1:] != (hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [tokens, {hkv}, {d}] with contiguous rows")
+    if key.shape[0] != value.shape[0] or slot_mapping.numel() < key.shape[0]:
+        raise ValueError("key, value and slot_mapping disagree on the token count")
+    if not (key.dtype == value.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("key, value and the pools must share one dtype")
+    rc = load().pa_reshape_and_cache(
+        _dev(key, "key"), _dev(value, "value"), key.stride(0), value.stride(0),
+        _contig(k_cache, "k_cache"), _contig(v_cache, "v_cache"),
+        _contig(slot_mapping, "slot_mapping", torch.int64), int(key.shape[0]), hkv, d,
+        block_size, num_blocks, _dtype_code(k_cache), _opt(dev_status), _stream(stream))
+    _check(rc, "pa_reshape_and_cache")
+
+
+def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                               block_size, max_blocks))
+
+
+def varlen_prefill_workspace_size(num_seqs, total_q, num_heads, num_kv_heads, head_dim, block_size,
+                                  max_blocks) -> int:
+    return int(load().pa_varlen_prefill_workspace_size(num_seqs, total_q, num_heads, num_kv_heads,
+                                                       head_dim, block_size, max_blocks))
+
+
+def _ws(workspace, nbytes, device):
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    return workspace
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,
+           workspace=None, dev_status=None, stream=None):
+    """pa_decode: q [num_seqs, H, D] -> out [num_seqs, H, D]."""
+    num_seqs, H, D = q.shape
+    num_blocks, block_size, hkv, d = k_cache.shape
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_workspace_size(num_seqs, H, hkv, D, block_size, max_blocks)
+    workspace = _ws(workspace, need, q.device)
+    rc = load().pa_decode(
+        _contig(out, "out"), _contig(q, "q"), _contig(k_cache, "k_cache"), _contig(v_cache, "v_cache"),
+        _contig(block_tables, "block_tables", torch.int32), _contig(context_lens, "context_lens", torch.int32),
+        num_seqs, H, hkv, D, block_size, max_blocks, num_blocks, float(scale), _dtype_code(q),
+        _contig(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _opt(dev_status), _stream(stream))
+    _check(rc, "pa_decode")
+    return out
+
+
+def varlen_prefill(q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                   max_q_len: int, out=None, workspace=None, dev_status=None, stream=None):
+    """pa_varlen_prefill over a concatenated super-sequence: q [total_q, H, D]."""
+    total_q, H, D = q.shape
+    num_blocks, block_size, hkv, d = k_cache.shape
+    num_seqs, max_blocks = block_tables.shape
+    if out is None:
+        out = torch.empty_like(q)
+    need = varlen_prefill_workspace_size(num_seqs, total_q, H, hkv, D, block_size, max_blocks)
+    workspace = _ws(workspace, need, q.device)
+    rc = load().pa_varlen_prefill(
+        _contig(out, "out"), _contig(q, "q"), _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32),
+        _contig(k_cache, "k_cache"), _contig(v_cache, "v_cache"),
+        _contig(block_tables, "block_tables", torch.int32), _contig(context_lens, "context_lens", torch.int32),
+        num_seqs, total_q, int(max_q_len), H, hkv, D, block_size, max_blocks, num_blocks, float(scale),
+        _dtype_code(q), _contig(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _opt(dev_status), _stream(stream))
+    _check(rc, "pa_varlen_prefill")
+    return out
+
+
+def get_device_status(dev_status, stream=None) -> int:
+    host = ctypes.c_int32(-1)
+    rc = load().pa_get_device_status(_dev(dev_status, "dev_status", torch.int32), ctypes.byref(host),
+                                     _stream(stream))
+    _check(rc, "pa_get_device_status")
+    return int(host.value)
+
+
+def reset_device_status(dev_status, stream=None) -> None:
+    _check(load().pa_reset_device_status(_dev(dev_status, "dev_status", torch.int32), _stream(stream)),
+           "pa_reset_device_status")
+
+
+def set_timing_events(ev_begin=None, ev_end=None) -> None:
+    """pa_set_timing_events with torch.cuda.Event objects (or None, None)."""
+    def handle(ev):
+        if ev is None:
+            return None
+        if ev.cuda_event == 0:      # torch creates the CUDA event on first record
+            ev.record()
+        return ev.cuda_event
+    _check(load().pa_set_timing_events(handle(ev_begin), handle(ev_end)), "pa_set_timing_events")

@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU fp64 oracle on the
+same seeded inputs.
+
+Bit-exact: slot mapping and the whole cache pool after the write.  Floating
+point: fp32 max |err| <= 1e-5; bf16 max |err| <= 2e-2 and relative RMS <= 1e-2.
+Small versions of every workload are compared on every output; the full-size
+workloads on every output where the oracle is quick and on a sample otherwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pagedattention_kv_cache_reshape_gb300 import pa
+from pagedattention_kv_cache_reshape_gb300 import workloads as W
+
+from helpers import (compare, gpu_step, oracle_attention, oracle_blocks, oracle_rows,
+                     oracle_write, to_f64)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from pagedattention_kv_cache_reshape_gb300 import build
+    build.build()
+    pa.load()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+SMALL = {
+    "tiny": lambda seed: W.tiny(seed, oracle_blocks, device=DEV),
+    "mha_small": lambda seed: W.mha(seed, oracle_blocks, num_seqs=6, ctx_lo=100, ctx_hi=300, device=DEV),
+    "gqa_small": lambda seed: W.gqa(seed, oracle_blocks, num_seqs=24, ctx_hi=700, shared_seqs=6,
+                                    prefix_tokens=128, device=DEV),
+    "long_small": lambda seed: W.long(seed, oracle_blocks, num_seqs=2, ctx=3000, num_blocks=420, device=DEV),
+    "mixed_small": lambda seed: W.mixed(seed, oracle_blocks, num_prefill=3, chunk=40, prefix_hi=70,
+                                        num_decode=9, dec_lo=5, dec_hi=300, device=DEV),
+    "mqa_small": lambda seed: W.build("mqa", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                      num_heads=8, num_kv_heads=1, head_dim=128, block_size=16,
+                                      q_lens=[1] * 5, context_lens=[1, 17, 230, 64, 999], device=DEV),
+    "d64_bf16": lambda seed: W.build("d64", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                     num_heads=16, num_kv_heads=4, head_dim=64, block_size=16,
+                                     q_lens=[1] * 7, context_lens=[5, 16, 33, 400, 2, 129, 1000], device=DEV),
+    "fp32_gqa_prefill": lambda seed: W.build("f32p", seed=seed, blocks_needed=oracle_blocks,
+                                             dtype=torch.float32, num_heads=8, num_kv_heads=2, head_dim=128,
+                                             block_size=16, q_lens=[20, 1, 7, 1], context_lens=[20, 60, 40, 1],
+                                             device=DEV),
+}
+
+
+def _cpu_copy(w):
+    return w.to("cpu")
+
+
+def _run_and_check_all(w, seeds_note=""):
+    wc = _cpu_copy(w)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots, out = gpu_step(w, dev_status=status)
+    torch.cuda.synchronize()
+    assert pa.get_device_status(status) == 0
+    ref_slots = oracle_write(wc)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots), "slot mapping differs"
+    assert torch.equal(w.k_cache.cpu().view(torch.int16 if w.dtype == torch.bfloat16 else torch.int32),
+                       wc.k_cache.view(torch.int16 if w.dtype == torch.bfloat16 else torch.int32))
+    assert torch.equal(w.v_cache.cpu().view(torch.int16 if w.dtype == torch.bfloat16 else torch.int32),
+                       wc.v_cache.view(torch.int16 if w.dtype == torch.bfloat16 else torch.int32))
+    ref = oracle_attention(wc)
+    return compare(to_f64(out), ref, w.dtype, w.name + seeds_note)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("seed", [1, 2])
+def test_small_workloads_every_output(name, seed):
+    _run_and_check_all(SMALL[name](seed), f" seed {seed}")
+
+
+def test_tiny_config_full():
+    # configuration: 4 sequences, context {1,16,17,50}, fp32, 32-block pool
+    for seed in (0, 3, 4):
+        _run_and_check_all(W.tiny(seed, oracle_blocks, device=DEV), f" seed {seed}")
+
+
+@pytest.mark.parametrize("name", ["mha64_bf16", "gqa256_bf16", "long_bf16"])
+def test_full_size_decode_every_output(name):
+    w = W.make(name, 0, oracle_blocks, device=DEV)
+    _run_and_check_all(w)
+
+
+def test_full_size_mixed_sampled():
+    w = W.make("mixed_bf16", 0, oracle_blocks, device=DEV)
+    wc = _cpu_copy(w)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots, out = gpu_step(w, dev_status=status)
+    torch.cuda.synchronize()
+    assert pa.get_device_status(status) == 0
+    ref_slots = oracle_write(wc)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    assert torch.equal(w.k_cache.cpu().view(torch.int16), wc.k_cache.view(torch.int16))
+    assert torch.equal(w.v_cache.cpu().view(torch.int16), wc.v_cache.view(torch.int16))
+    # every decode row, and the first, last and 14 random rows of every chunk, all heads
+    cu = wc.cu_seqlens_q.numpy()
+    ql = cu[1:] - cu[:-1]
+    rng = np.random.default_rng(0)
+    rows = []
+    for s in range(len(ql)):
+        if ql[s] == 1:
+            rows.append(cu[s])
+        else:
+            rows.extend([cu[s], cu[s + 1] - 1, *rng.integers(cu[s], cu[s + 1], 14).tolist()])
+    rows = np.unique(np.array(rows))
+    H = w.num_heads
+    rr = np.repeat(rows, H)
+    hh = np.tile(np.arange(H), rows.size)
+    ref = oracle_rows(wc, rr, hh)
+    got = to_f64(out)[rr, hh]
+    compare(got, ref, w.dtype, "mixed_bf16 sampled")
+
+
+def _poison_unused(w):
+    """NaN into every pool slot no sequence reads: unreferenced blocks and the
+    tail of each sequence's last block (live slots found with the oracle)."""
+    wc = _cpu_copy(w)
+    slots = []
+    for s in range(w.num_seqs):
+        c = int(wc.context_lens[s])
+        cu = torch.tensor([0, c], dtype=torch.int32)
+        slots.append(oracle.slot_mapping(wc.block_tables[s:s + 1], torch.zeros(1, dtype=torch.int32),
+                                         cu, w.block_size, w.num_blocks))
+    live = np.unique(np.concatenate(slots))
+    mask = torch.ones(w.num_blocks * w.block_size, dtype=torch.bool)
+    mask[torch.from_numpy(live)] = False
+    mask = mask.to(DEV)
+    for pool in (w.k_cache, w.v_cache):
+        pool.view(w.num_blocks * w.block_size, -1)[mask] = float("nan")
+
+
+@pytest.mark.parametrize("name", ["gqa_small", "mixed_small", "tiny", "mha_small"])
+def test_nan_poison_in_unused_slots_never_reaches_output(name):
+    clean = SMALL[name](5)
+    _, out_clean = gpu_step(clean)
+    dirty = SMALL[name](5)
+    _poison_unused(dirty)
+    _, out_dirty = gpu_step(dirty)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out_dirty.float()).all()
+    assert torch.equal(out_clean, out_dirty)
+
+
+@pytest.mark.parametrize("name", ["gqa_small", "long_small", "mixed_small"])
+def test_block_permutation_bitwise_invariance(name):
+    w = SMALL[name](7)
+    _, base = gpu_step(w)          # writes the new tokens into w's pools
+    out_before = base.clone()
+    # move every block to a new physical id and renumber the tables
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(3)).to(DEV)
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    bt = w.block_tables.clone()
+    live = bt >= 0
+    bt[live] = perm[bt[live].long()].to(torch.int32)
+    if w.decode_only:
+        out = pa.decode(w.q, k2, v2, bt, w.context_lens, w.scale)
+    else:
+        out = pa.varlen_prefill(w.q, w.cu_seqlens_q, k2, v2, bt, w.context_lens, w.scale,
+                                int(w.q_lens.max()))
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_before)
+
+
+def test_run_to_run_determinism():
+    w = W.make("gqa256_bf16", 1, oracle_blocks, device=DEV)
+    _, a = gpu_step(w)
+    outs = [pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, a)
+
+
+def test_shared_prefix_identical_outputs():
+    w = W.gqa(11, oracle_blocks, num_seqs=8, ctx_hi=600, shared_seqs=4, prefix_tokens=256, device=DEV)
+    # sequences 1..3 become copies of sequence 0: same context, same query,
+    # the shared prefix blocks plus private copies of 0's other blocks
+    pb = 256 // 16
+    ctx0 = int(w.context_lens[0])
+    nb0 = w.blocks_per_seq[0]
+    w.context_lens[1:4] = ctx0
+    # give 1..3 private copies of 0's private blocks
+    free = sorted(set(range(w.num_blocks)) - set(w.block_tables[w.block_tables >= 0].tolist()))
+    bt = w.block_tables.clone()
+    cursor = 0
+    for s in (1, 2, 3):
+        bt[s, :] = -1
+        bt[s, :pb] = w.block_tables[0, :pb]
+        for lb in range(pb, nb0):
+            nb = free[cursor]
+            cursor += 1
+            bt[s, lb] = nb
+            w.k_cache[nb] = w.k_cache[w.block_tables[0, lb]]
+            w.v_cache[nb] = w.v_cache[w.block_tables[0, lb]]
+    w.block_tables = bt.contiguous()
+    w.q[1:4] = w.q[0]
+    kb, vb = w.k_cache.clone(), w.v_cache.clone()
+    out = pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
+    torch.cuda.synchronize()
+    for s in (1, 2, 3):
+        assert torch.equal(out[s], out[0])
+    assert torch.equal(kb.view(torch.int16), w.k_cache.view(torch.int16))
+    assert torch.equal(vb.view(torch.int16), w.v_cache.view(torch.int16))
+
+
+def test_prefill_row_matches_decode_at_same_position():
+    w = W.build("t6", seed=9, blocks_needed=oracle_blocks, dtype=torch.bfloat16, num_heads=32,
+                num_kv_heads=8, head_dim=128, block_size=16, q_lens=[70], context_lens=[70], device=DEV)
+    _, pre = gpu_step(w)
+    for i in (0, 15, 16, 40, 69):
+        dec = pa.decode(w.q[i:i + 1].contiguous(), w.k_cache, w.v_cache, w.block_tables,
+                        torch.tensor([i + 1], dtype=torch.int32, device=DEV), w.scale)
+        torch.cuda.synchronize()
+        compare(to_f64(dec[0]), to_f64(pre[i]), torch.bfloat16, f"row {i}")
+
+
+def test_token_strided_fused_qkv_write():
+    w = SMALL["gqa_small"](4)
+    T, hkv, d = w.key.shape
+    fused = torch.empty(T, 3, hkv, d, dtype=w.dtype, device=DEV)
+    fused[:, 0] = 0
+    fused[:, 1] = w.key
+    fused[:, 2] = w.value
+    ref = SMALL["gqa_small"](4)
+    slots = pa.compute_slot_mapping(w.block_tables, w.seq_start, w.cu_seqlens_q, w.num_blocks, w.total_q)
+    pa.reshape_and_cache(fused[:, 1], fused[:, 2], w.k_cache, w.v_cache, slots)
+    pa.reshape_and_cache(ref.key, ref.value, ref.k_cache, ref.v_cache, slots)
+    torch.cuda.synchronize()
+    assert torch.equal(w.k_cache.view(torch.int16), ref.k_cache.view(torch.int16))
+    assert torch.equal(w.v_cache.view(torch.int16), ref.v_cache.view(torch.int16))
+
+
+def test_negative_slot_is_skipped_and_out_of_range_slot_flagged():
+    w = SMALL["mha_small"](2)
+    before_k = w.k_cache.clone()
+    slots = torch.full((w.total_q,), -1, dtype=torch.int64, device=DEV)
+    slots[0] = 5
+    slots[1] = w.num_blocks * 16            # outside the pool
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.reshape_and_cache(w.key, w.value, w.k_cache, w.v_cache, slots, dev_status=status)
+    assert pa.get_device_status(status) == pa.ERR_OUT_OF_RANGE
+    changed = (w.k_cache != before_k).view(w.num_blocks * 16, -1).any(1)
+    assert changed.nonzero().flatten().tolist() == [5]
+
+
+def test_out_of_range_block_id_sets_status_without_fault():
+    w = SMALL["gqa_small"](3)
+    gpu_step(w)
+    bt = w.block_tables.clone()
+    bt[2, 0] = w.num_blocks + 100
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.decode(w.q, w.k_cache, w.v_cache, bt, w.context_lens, w.scale, dev_status=status)
+    assert pa.get_device_status(status) == pa.ERR_OUT_OF_RANGE
+    # slot mapping over a bad entry: slot -1 and the status
+    status.zero_()
+    ss = torch.tensor([0], dtype=torch.int32, device=DEV)
+    cu = torch.tensor([0, 3], dtype=torch.int32, device=DEV)
+    s = pa.compute_slot_mapping(bt[2:3].contiguous(), ss, cu, w.num_blocks, 3, dev_status=status)
+    assert pa.get_device_status(status) == pa.ERR_OUT_OF_RANGE
+    assert s.tolist() == [-1, -1, -1]
+
+
+def test_zero_context_flags_and_leaves_row_untouched():
+    w = SMALL["gqa_small"](6)
+    gpu_step(w)
+    ctx = w.context_lens.clone()
+    ctx[5] = 0
+    out = torch.full_like(w.q, 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, ctx, w.scale, out=out, dev_status=status)
+    assert pa.get_device_status(status) == pa.ERR_OUT_OF_RANGE
+    assert (out[5] == 7.0).all()
+    assert torch.isfinite(out.float()).all()
+
+
+def test_workspace_too_small_is_rejected():
+    w = SMALL["gqa_small"](1)
+    ws = torch.empty(64, dtype=torch.uint8, device=DEV)
+    with pytest.raises(pa.PAError) as e:
+        pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, workspace=ws)
+    assert e.value.status == pa.ERR_WORKSPACE
