@@ -274,7 +274,16 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         graph = g
 
-    flush = torch.empty(2 * L2_BYTES // 4 * 2, dtype=torch.float32, device=dev)   # ~258 MB > L2
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)   # 258 MB, 2x L2
+    evict = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    evict.zero_()
+    evict_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write 2x L2 of unrelated data, then read another 2x L2 so the lines
+        # left in L2 are clean (no write-back of the flush inside the timed step)
+        flush.zero_()
+        torch.sum(evict, dim=0, out=evict_sum)
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -288,7 +297,7 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
         for i in range(K):
-            flush.zero_()
+            flush_l2()
             if graph is not None:
                 ev[i][0].record(stream)
                 graph.replay()
@@ -311,7 +320,7 @@ def run_ours(args, world, rank, local):
     # library records around that launch on the launching stream (direct launches)
     kern_ms = []
     for i in range(min(K, 100)):
-        flush.zero_()
+        flush_l2()
         pa.set_timing_events(*kev[i])
         step()
     pa.set_timing_events(None, None)
@@ -333,7 +342,7 @@ def run_ours(args, world, rank, local):
         K2 = min(K, 100)
         e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
         for i in range(K2 + 3):
-            flush.zero_()
+            flush_l2()
             if i >= 3:
                 e_ev[i - 3][0].record(stream)
             for k in host:
@@ -407,7 +416,7 @@ def main():
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
             "num_blocks": w.num_blocks, "context_tokens": b["logical_tokens"],
             "unique_context_tokens": b["unique_tokens"], "query_tokens": w.total_q,
-            "l2": "flushed before every timed step (258 MB write)",
+            "l2": "flushed before every timed step: 258 MB written, then 258 MB read (clean lines)",
             "launch": "CUDA graph of the step's kernels" if r["graph"] else "direct launches",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },

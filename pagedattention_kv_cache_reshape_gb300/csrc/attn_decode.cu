@@ -458,14 +458,21 @@ __global__ void __launch_bounds__(256)
     const int64_t c0 = cta_of(hg * T + b0, NV, num_ctas);
     const int64_t c1 = cta_of(hg * T + b1 - 1, NV, num_ctas);
     if (c0 == c1) return;  // whole sequence inside one CTA: already written
+    // CTAs with an empty slice (possible when the batch has fewer blocks than
+    // CTAs) wrote nothing: their slots hold stale workspace contents.
+    auto has_slice = [&](int64_t c) {
+        return cta_slice_begin(c, NV, num_ctas) < cta_slice_begin(c + 1, NV, num_ctas);
+    };
     float M = -INFINITY;
-    for (int64_t c = c0; c <= c1; ++c) M = fmaxf(M, p.part_ml[((vs + c) * p.qh + h_loc) * 2]);
+    for (int64_t c = c0; c <= c1; ++c)
+        if (has_slice(c)) M = fmaxf(M, p.part_ml[((vs + c) * p.qh + h_loc) * 2]);
     constexpr int kPer = D / 32;
     float acc[kPer];
 #pragma unroll
     for (int t = 0; t < kPer; ++t) acc[t] = 0.f;
     float L = 0.f;
     for (int64_t c = c0; c <= c1; ++c) {
+        if (!has_slice(c)) continue;
         const int64_t slot = vs + c;
         const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2);
         const float w = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);

@@ -181,27 +181,20 @@ def test_run_to_run_determinism():
 
 
 def test_shared_prefix_identical_outputs():
-    w = W.gqa(11, oracle_blocks, num_seqs=8, ctx_hi=600, shared_seqs=4, prefix_tokens=256, device=DEV)
-    # sequences 1..3 become copies of sequence 0: same context, same query,
-    # the shared prefix blocks plus private copies of 0's other blocks
+    """Sequences 0..3 reference the same 256-token prefix blocks read-only and
+    hold identical private tails and queries: identical outputs, pool unchanged."""
+    ctx = [300, 300, 300, 300, 57, 610, 16, 140]
+    w = W.build("shared", seed=11, blocks_needed=oracle_blocks, dtype=torch.bfloat16, num_heads=32,
+                num_kv_heads=8, head_dim=128, block_size=16, q_lens=[1] * 8, context_lens=ctx,
+                shared_prefix_seqs=4, shared_prefix_tokens=256, device=DEV)
     pb = 256 // 16
-    ctx0 = int(w.context_lens[0])
-    nb0 = w.blocks_per_seq[0]
-    w.context_lens[1:4] = ctx0
-    # give 1..3 private copies of 0's private blocks
-    free = sorted(set(range(w.num_blocks)) - set(w.block_tables[w.block_tables >= 0].tolist()))
-    bt = w.block_tables.clone()
-    cursor = 0
+    bt = w.block_tables
+    assert torch.equal(bt[1, :pb], bt[0, :pb])
     for s in (1, 2, 3):
-        bt[s, :] = -1
-        bt[s, :pb] = w.block_tables[0, :pb]
-        for lb in range(pb, nb0):
-            nb = free[cursor]
-            cursor += 1
-            bt[s, lb] = nb
-            w.k_cache[nb] = w.k_cache[w.block_tables[0, lb]]
-            w.v_cache[nb] = w.v_cache[w.block_tables[0, lb]]
-    w.block_tables = bt.contiguous()
+        for lb in range(pb, w.blocks_per_seq[0]):
+            assert int(bt[s, lb]) != int(bt[0, lb])
+            w.k_cache[bt[s, lb]] = w.k_cache[bt[0, lb]]
+            w.v_cache[bt[s, lb]] = w.v_cache[bt[0, lb]]
     w.q[1:4] = w.q[0]
     kb, vb = w.k_cache.clone(), w.v_cache.clone()
     out = pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
@@ -210,6 +203,8 @@ def test_shared_prefix_identical_outputs():
         assert torch.equal(out[s], out[0])
     assert torch.equal(kb.view(torch.int16), w.k_cache.view(torch.int16))
     assert torch.equal(vb.view(torch.int16), w.v_cache.view(torch.int16))
+    wc = w.to("cpu")
+    compare(to_f64(out), oracle_attention(wc), torch.bfloat16, "shared prefix")
 
 
 def test_prefill_row_matches_decode_at_same_position():
@@ -280,6 +275,21 @@ def test_zero_context_flags_and_leaves_row_untouched():
     assert pa.get_device_status(status) == pa.ERR_OUT_OF_RANGE
     assert (out[5] == 7.0).all()
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name", ["gqa_small", "mixed_small", "long_small", "mha_small"])
+def test_stale_workspace_contents_do_not_matter(name):
+    """The workspace may hold anything on entry (here: NaN bytes everywhere)."""
+    w = SMALL[name](8)
+    _, clean = gpu_step(w)
+    ws_bytes = (pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, 16, w.max_blocks)
+                if w.decode_only else
+                pa.varlen_prefill_workspace_size(w.num_seqs, w.total_q, w.num_heads, w.num_kv_heads,
+                                                 w.head_dim, 16, w.max_blocks))
+    ws = torch.full((ws_bytes,), 0xFF, dtype=torch.uint8, device=DEV)     # NaN patterns
+    _, dirty = gpu_step(w, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(clean, dirty)
 
 
 def test_workspace_too_small_is_rejected():
