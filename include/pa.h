@@ -164,6 +164,34 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const 
                     void *workspace, size_t workspace_bytes, int32_t *dev_status,
                     pa_stream_t stream);
 
+/*
+ * Decode without a caller workspace.  The paper has no counterpart: this is a
+ * convenience for callers that cannot allocate device memory -- for example a
+ * plugin interface that only hands over input and output pointers, or a
+ * serving process whose memory pool has already claimed the device's free
+ * memory for the KV cache.  Same arguments and results as pa_decode, minus
+ * the workspace.
+ *
+ * The scratch is a fixed PA_STATIC_SCRATCH_BYTES (24 MiB) array inside the
+ * library: every GPU that loads the library holds it until the process
+ * exits.  A problem whose pa_decode_workspace_size(...) exceeds it returns
+ * PA_ERR_WORKSPACE before anything is launched.  The call allocates nothing.
+ * The first call on each device looks up the array's device address with a
+ * synchronous CUDA runtime call, so make that first call before any stream
+ * capture.  Every call shares the one array and leaves its last contents
+ * there; nothing in it has to start at zero.  Calls that can overlap on the
+ * GPU (different streams, or several devices' threads targeting one device)
+ * race on the array: serialise them.
+ */
+#define PA_STATIC_SCRATCH_BYTES ((size_t)24 << 20)
+PA_API pa_status pa_decode_static_scratch(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, int num_seqs,
+                                          int num_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int max_blocks, int num_blocks,
+                                          float scale, pa_dtype dtype, int32_t *dev_status,
+                                          pa_stream_t stream);
+
 /* Workspace bytes pa_varlen_prefill needs for these sizes. */
 PA_API size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
                                         int num_kv_heads, int head_dim, int block_size,

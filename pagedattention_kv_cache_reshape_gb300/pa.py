@@ -25,8 +25,9 @@ EXPORTS = (
     "pa_status_string", "pa_version", "pa_num_blocks_needed", "pa_compute_slot_mapping",
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
     "pa_varlen_prefill_workspace_size", "pa_varlen_prefill", "pa_get_device_status",
-    "pa_reset_device_status", "pa_set_timing_events",
+    "pa_reset_device_status", "pa_set_timing_events", "pa_decode_static_scratch",
 )
+STATIC_SCRATCH_BYTES = 24 << 20
 
 
 class PAError(RuntimeError):
@@ -75,6 +76,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_reset_device_status.argtypes = [vp, vp]
         L.pa_set_timing_events.restype = i32
         L.pa_set_timing_events.argtypes = [vp, vp]
+        L.pa_decode_static_scratch.restype = i32
+        L.pa_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                               f32, i32, vp, vp]
         _lib = L
         return L
 
@@ -245,3 +249,21 @@ def set_timing_events(ev_begin=None, ev_end=None) -> None:
             ev.record()
         return ev.cuda_event
     _check(load().pa_set_timing_events(handle(ev_begin), handle(ev_end)), "pa_set_timing_events")
+
+
+def decode_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,
+                          dev_status=None, stream=None):
+    """pa_decode_static_scratch: pa_decode with the library's fixed scratch array
+    (for callers that cannot allocate device memory)."""
+    num_seqs, H, D = q.shape
+    num_blocks, block_size, hkv, d = k_cache.shape
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    rc = load().pa_decode_static_scratch(
+        _contig(out, "out"), _contig(q, "q"), _contig(k_cache, "k_cache"), _contig(v_cache, "v_cache"),
+        _contig(block_tables, "block_tables", torch.int32), _contig(context_lens, "context_lens", torch.int32),
+        num_seqs, H, hkv, D, block_size, max_blocks, num_blocks, float(scale), _dtype_code(q),
+        _opt(dev_status), _stream(stream))
+    _check(rc, "pa_decode_static_scratch")
+    return out
