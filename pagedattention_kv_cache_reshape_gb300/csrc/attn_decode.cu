@@ -489,20 +489,6 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 // Pool [num_blocks][16][Hkv][D] bf16 seen as a 5-D tensor whose box is one
 // block for `box_heads` kv-heads, laid out in shared memory as
 // [head][D/64][token][64] with 128-byte rows and the 128-byte swizzle.
@@ -565,16 +551,16 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
 
 template <int D>
 cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtensorMap &mk,
-                        const CUtensorMap &mv, int grid, cudaStream_t stream) {
+                        const CUtensorMap &mv, int grid, cudaStream_t stream, bool timed) {
     const int kv_tile = prm.kvh * kB * D * 2;
     const int stage_bytes = (int)align_up(2 * kv_tile + prm.qh * D * 2, 1024);
     const size_t smem = 1024 + (size_t)prm.num_stages * (stage_bytes + sizeof(StageHeader) + 16);
     auto kern = split_decode_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    timing_begin(stream);
+    if (timed) timing_begin(stream);
     kern<<<grid, 32 * (prm.kvh + 1), smem, stream>>>(mk, mv, prm);
-    timing_end(stream);
+    if (timed) timing_end(stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int warps = prm.nhg * prm.num_seqs * prm.qh;
@@ -610,7 +596,7 @@ size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max
 }
 
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, bool timed) {
     if (a.num_seqs == 0) return cudaSuccess;
     const WorkspaceLayout w = workspace_layout(a.num_seqs, a.num_heads, a.head_dim, a.max_blocks);
     if (workspace_bytes < w.total) return cudaErrorInvalidValue;
@@ -665,8 +651,8 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
 
     int grid = sms;
     if (grid > kPartialCtas) grid = kPartialCtas;
-    return a.head_dim == 64 ? launch_main<64>(a, prm, mk, mv, grid, stream)
-                            : launch_main<128>(a, prm, mk, mv, grid, stream);
+    return a.head_dim == 64 ? launch_main<64>(a, prm, mk, mv, grid, stream, timed)
+                            : launch_main<128>(a, prm, mk, mv, grid, stream, timed);
 }
 
 }  // namespace pa

@@ -23,7 +23,7 @@ constexpr int kMaxGroup = 32;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
-    generic_attention_kernel(AttnArgs a, bool skip_single_row) {
+    generic_attention_kernel(AttnArgs a, int row_filter) {
     extern __shared__ float smem[];
     const int G = a.num_heads / a.num_kv_heads;
     float *q_s = smem;                  // [G][D]
@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(kThreads)
         q_len = 1;
     }
     const int i = row - first;
-    if (skip_single_row && q_len == 1) return;
+    if ((row_filter == kSkipSingleRows && q_len == 1) || (row_filter == kOnlySingleRows && q_len != 1))
+        return;
     const int ctx = __ldg(a.context_lens + s);
     if (i < 0 || i >= q_len || ctx <= 0 || (int64_t)ctx > (int64_t)a.max_blocks * a.block_size ||
         q_len > ctx || q_len > a.max_q_len) {
@@ -175,31 +176,28 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <typename T, int D>
-cudaError_t launch_typed(const AttnArgs &a, bool skip_single_row, cudaStream_t stream) {
+cudaError_t launch_typed(const AttnArgs &a, int row_filter, cudaStream_t stream) {
     const int G = a.num_heads / a.num_kv_heads;
     const size_t smem = sizeof(float) * (2 * G * D + G * kTile + 3 * G) + sizeof(int) * kTile;
     auto kern = generic_attention_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.total_q, a.num_kv_heads);
-    if (!skip_single_row) timing_begin(stream);
-    kern<<<grid, kThreads, smem, stream>>>(a, skip_single_row);
-    if (!skip_single_row) timing_end(stream);
+    kern<<<grid, kThreads, smem, stream>>>(a, row_filter);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_generic_attention(const AttnArgs &a, bool skip_single_row,
-                                     cudaStream_t stream) {
+cudaError_t launch_generic_attention(const AttnArgs &a, int row_filter, cudaStream_t stream) {
     if (a.total_q == 0 || a.num_seqs == 0) return cudaSuccess;
     if (a.num_heads / a.num_kv_heads > kMaxGroup) return cudaErrorInvalidValue;
     if (a.dtype == PA_DTYPE_F32) {
-        return a.head_dim == 64 ? launch_typed<float, 64>(a, skip_single_row, stream)
-                                : launch_typed<float, 128>(a, skip_single_row, stream);
+        return a.head_dim == 64 ? launch_typed<float, 64>(a, row_filter, stream)
+                                : launch_typed<float, 128>(a, row_filter, stream);
     }
-    return a.head_dim == 64 ? launch_typed<__nv_bfloat16, 64>(a, skip_single_row, stream)
-                            : launch_typed<__nv_bfloat16, 128>(a, skip_single_row, stream);
+    return a.head_dim == 64 ? launch_typed<__nv_bfloat16, 64>(a, row_filter, stream)
+                            : launch_typed<__nv_bfloat16, 128>(a, row_filter, stream);
 }
 
 }  // namespace pa

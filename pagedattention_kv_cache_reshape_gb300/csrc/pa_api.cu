@@ -31,6 +31,20 @@ namespace {
 thread_local cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
 void timing_begin(cudaStream_t stream) {
     if (g_ev_begin && g_ev_end) cudaEventRecord(g_ev_begin, stream);
 }
@@ -168,17 +182,22 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
         const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
                                                      block_size, max_blocks);
         if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
-        return from_cuda(launch_split_decode(a, workspace, workspace_bytes, s));
+        return from_cuda(launch_split_decode(a, workspace, workspace_bytes, s, true));
     }
-    return from_cuda(launch_generic_attention(a, false, s));
+    timing_begin(s);
+    const cudaError_t e = launch_generic_attention(a, kAllRows, s);
+    timing_end(s);
+    return from_cuda(e);
 }
 
 size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
                                         int num_kv_heads, int head_dim, int block_size,
                                         int max_blocks) {
-    (void)total_q;
+    if (total_q < 0) total_q = 0;
+    if (num_seqs < 0) num_seqs = 0;
     return pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                                    max_blocks);
+                                    max_blocks) +
+           prefill_workspace(num_seqs, total_q);
 }
 
 pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_q,
@@ -202,19 +221,34 @@ pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_
                num_seqs, total_q, max_q_len, num_heads, num_kv_heads, head_dim, block_size,
                max_blocks, num_blocks, scale, dtype, dev_status};
     cudaStream_t s = (cudaStream_t)stream;
-    if (split_decode_supported(a)) {
+    const bool fast_decode = split_decode_supported(a);
+    const bool fast_prefill = prefill_tc_supported(a);
+    const size_t dec_ws = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                   block_size, max_blocks);
+    if (fast_decode || fast_prefill) {
         const size_t need = pa_varlen_prefill_workspace_size(num_seqs, total_q, num_heads,
                                                              num_kv_heads, head_dim, block_size,
                                                              max_blocks);
         if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
-        // decode rows (q_len == 1) stream through the split-KV decode kernels,
-        // the prefill chunks through the attention kernel
-        cudaError_t e = launch_split_decode(a, workspace, workspace_bytes, s);
-        if (e != cudaSuccess) return from_cuda(e);
-        if (max_q_len <= 1) return PA_OK;
-        return from_cuda(launch_generic_attention(a, true, s));
     }
-    return from_cuda(launch_generic_attention(a, false, s));
+    // decode rows (q_len == 1) stream through the split-KV decode kernels,
+    // prefill chunks (q_len >= 2) through the tensor-core prefill kernel
+    timing_begin(s);
+    cudaError_t e = cudaSuccess;
+    if (fast_decode) {
+        e = launch_split_decode(a, workspace, dec_ws, s, false);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    if (max_q_len > 1 || !fast_decode) {
+        if (fast_prefill && max_q_len > 1) {
+            e = launch_prefill_tc(a, static_cast<uint8_t *>(workspace) + dec_ws, workspace_bytes - dec_ws, s);
+            if (e == cudaSuccess && !fast_decode) e = launch_generic_attention(a, kOnlySingleRows, s);
+        } else {
+            e = launch_generic_attention(a, fast_decode ? kSkipSingleRows : kAllRows, s);
+        }
+    }
+    timing_end(s);
+    return from_cuda(e);
 }
 
 pa_status pa_get_device_status(const int32_t *dev_status, int32_t *host_out, pa_stream_t stream) {

@@ -1,6 +1,8 @@
 // pa_internal.h -- launchers shared between the library's translation units.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -37,6 +39,10 @@ constexpr int kMaxPersistentCtas = 1024;
 
 int device_sm_count();  // SM count of the current device (cached per device)
 
+// cuTensorMapEncodeTiled from the driver, found through the runtime (the
+// library does not link libcuda); nullptr if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 // Timing hook (pa_set_timing_events): records the caller's events, if set,
 // around the main attention kernel.
 void timing_begin(cudaStream_t stream);
@@ -55,10 +61,9 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                                      cudaStream_t stream);
 
 // CUDA-core attention for every supported shape and dtype (one CTA per query
-// row and kv-head).  With skip_single_row, sequences whose q_len is 1 are left
-// to the decode kernels.
-cudaError_t launch_generic_attention(const AttnArgs &a, bool skip_single_row,
-                                     cudaStream_t stream);
+// row and kv-head).  row_filter selects the sequences it computes.
+constexpr int kAllRows = 0, kSkipSingleRows = 1, kOnlySingleRows = 2;
+cudaError_t launch_generic_attention(const AttnArgs &a, int row_filter, cudaStream_t stream);
 
 // Persistent TMA + tensor-core split-KV decode (bf16, head_dim 64/128).
 bool split_decode_supported(const AttnArgs &a);
@@ -66,6 +71,13 @@ size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max
 // With a.cu_seqlens_q set, only sequences with q_len == 1 are processed and
 // their query/output row is cu_seqlens_q[s].
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool timed);
+
+// tcgen05 causal prefill for sequences with q_len >= 2 (bf16, head_dim 64/128,
+// q-heads per kv-head a power of two up to 16).
+bool prefill_tc_supported(const AttnArgs &a);
+size_t prefill_workspace(int num_seqs, int total_q);
+cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
 
 }  // namespace pa

@@ -76,6 +76,26 @@ def test_small_workloads_every_output(name, seed):
     _run_and_check_all(SMALL[name](seed), f" seed {seed}")
 
 
+PREFILL_CASES = {
+    # name: (H, Hkv, D, q_lens, context_lens)
+    "gqa4_mixed_lengths": (32, 8, 128, [300, 1, 7, 129, 2, 64], [300, 90, 1000, 129, 2, 2100]),
+    "mha_g1": (8, 8, 128, [130, 17, 1], [400, 17, 33]),
+    "g2": (8, 4, 128, [65, 3], [700, 50]),
+    "g8": (16, 2, 128, [40, 16], [333, 16]),
+    "g16": (16, 1, 128, [9, 25, 8], [9, 600, 300]),
+    "d64_gqa": (16, 4, 64, [100, 33, 1], [517, 33, 260]),
+    "long_prefix": (32, 8, 128, [48], [3000]),
+}
+
+
+@pytest.mark.parametrize("name", list(PREFILL_CASES))
+def test_prefill_shapes_every_output(name):
+    H, Hkv, D, ql, ctx = PREFILL_CASES[name]
+    w = W.build(name, seed=13, blocks_needed=oracle_blocks, dtype=torch.bfloat16, num_heads=H,
+                num_kv_heads=Hkv, head_dim=D, block_size=16, q_lens=ql, context_lens=ctx, device=DEV)
+    _run_and_check_all(w)
+
+
 def test_tiny_config_full():
     # configuration: 4 sequences, context {1,16,17,50}, fp32, 32-block pool
     for seed in (0, 3, 4):
