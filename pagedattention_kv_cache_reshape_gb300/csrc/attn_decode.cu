@@ -23,8 +23,11 @@
 //    with an online softmax (running max / sum, base-2 exponent) in fp32.
 //    A sequence slice wholly inside one CTA is normalised and stored; a
 //    sequence cut by CTA boundaries leaves (m, l, o) partials.
-//  * reduce kernel -- merges the partials of cut sequences:
+//  * reduce kernel -- merges the partials of cut sequences in CTA order:
 //        M = max m_i, L = sum l_i 2^{m_i - M}, o = sum 2^{m_i - M} o_i / L.
+// The three kernels are launched as programmatic dependents: each is resident
+// early and waits (griddepcontrol.wait) for its predecessor's results only
+// after its prologue, so launch latency overlaps the previous kernel.
 // Every cache byte is read once from HBM; the partition depends only on
 // context_lens and the CTA count, so results are bitwise reproducible and do
 // not depend on which physical blocks hold the data.
@@ -33,6 +36,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <utility>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -80,6 +84,13 @@ struct DecodeParams {
     int32_t *status;
 };
 
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ plan
 __global__ void __launch_bounds__(kPlanThreads)
     decode_plan_kernel(const int32_t *__restrict__ context_lens,
@@ -90,6 +101,8 @@ __global__ void __launch_bounds__(kPlanThreads)
     extern __shared__ int32_t pref_s[];  // [num_seqs + 1]
     __shared__ int32_t warp_tot[kPlanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dependency_wait();      // inputs may come from the previous kernel
+    grid_dependents_launch();    // the decode kernel may start its prologue
     int running = 0;
     for (int base = 0; base < num_seqs; base += kPlanThreads) {
         const int s = base + tid;
@@ -197,6 +210,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
+    grid_dependency_wait();      // the plan (and everything before it) is complete
+    grid_dependents_launch();    // the reduce kernel may become resident
 
     const int S = p.num_seqs;
     const int64_t T = __ldg(p.prefix + S);
@@ -442,9 +457,14 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
 }
 
 // ------------------------------------------------------------------ reduce
+// One warp per (virtual sequence, q-head) of a cut sequence.  Pieces are
+// combined in CTA order with the online rule (M, L, acc) <- (max, L a + l b,
+// acc a + o b), a = 2^{M - M'}, b = 2^{m - M'}; four pieces' loads are in
+// flight at a time.
 template <int D>
 __global__ void __launch_bounds__(256)
     split_decode_reduce_kernel(const DecodeParams p, int num_ctas) {
+    grid_dependency_wait();  // the decode kernel's partials are complete
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.num_seqs;
@@ -453,39 +473,49 @@ __global__ void __launch_bounds__(256)
     const int hg = vs / S, s = vs % S;
     const int64_t T = __ldg(p.prefix + S);
     const int64_t NV = T * p.nhg;
+    const int64_t P = num_ctas;
     const int64_t b0 = __ldg(p.prefix + s), b1 = __ldg(p.prefix + s + 1);
     if (b1 == b0) return;
-    const int64_t c0 = cta_of(hg * T + b0, NV, num_ctas);
-    const int64_t c1 = cta_of(hg * T + b1 - 1, NV, num_ctas);
+    const int64_t c0 = cta_of(hg * T + b0, NV, P);
+    const int64_t c1 = cta_of(hg * T + b1 - 1, NV, P);
     if (c0 == c1) return;  // whole sequence inside one CTA: already written
-    // CTAs with an empty slice (possible when the batch has fewer blocks than
-    // CTAs) wrote nothing: their slots hold stale workspace contents.
-    auto has_slice = [&](int64_t c) {
-        return cta_slice_begin(c, NV, num_ctas) < cta_slice_begin(c + 1, NV, num_ctas);
-    };
-    float M = -INFINITY;
-    for (int64_t c = c0; c <= c1; ++c)
-        if (has_slice(c)) M = fmaxf(M, p.part_ml[((vs + c) * p.qh + h_loc) * 2]);
     constexpr int kPer = D / 32;
-    float acc[kPer];
+    constexpr int kBatch = 4;
+    float M = -INFINITY, L = 0.f, acc[kPer];
 #pragma unroll
-    for (int t = 0; t < kPer; ++t) acc[t] = 0.f;
-    float L = 0.f;
-    for (int64_t c = c0; c <= c1; ++c) {
-        if (!has_slice(c)) continue;
-        const int64_t slot = vs + c;
-        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2);
-        const float w = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-        L += ml.y * w;
-        const float *src = p.part_o + (slot * p.qh + h_loc) * D;
+    for (int u = 0; u < kPer; ++u) acc[u] = 0.f;
+    for (int64_t cb = c0; cb <= c1; cb += kBatch) {
+        float2 ml[kBatch];
+        float ov[kBatch][kPer];
+        bool use[kBatch];
 #pragma unroll
-        for (int t = 0; t < kPer; ++t) acc[t] = fmaf(w, src[lane + 32 * t], acc[t]);
+        for (int k = 0; k < kBatch; ++k) {
+            const int64_t c = cb + k;
+            // CTAs with an empty slice (fewer blocks than CTAs) wrote nothing
+            use[k] = c <= c1 && (NV >= P || cta_slice_begin(c, NV, P) < cta_slice_begin(c + 1, NV, P));
+            const int64_t slot = vs + (use[k] ? c : c0);
+            ml[k] = *reinterpret_cast<const float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2);
+            const float *src = p.part_o + (slot * p.qh + h_loc) * D + lane * kPer;
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) ov[k][u] = src[u];
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            if (!use[k] || ml[k].x == -INFINITY) continue;
+            const float Mn = fmaxf(M, ml[k].x);
+            const float a = fast_exp2(M - Mn), b = fast_exp2(ml[k].x - Mn);
+            L = L * a + ml[k].y * b;
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) acc[u] = acc[u] * a + ov[k][u] * b;
+            M = Mn;
+        }
     }
     const int qrow = __ldg(&p.stream[b0].qrow);
-    __nv_bfloat16 *dst = p.out + ((int64_t)qrow * p.num_heads + (int64_t)hg * p.qh + h_loc) * D;
+    __nv_bfloat16 *dst = p.out + ((int64_t)qrow * p.num_heads + (int64_t)hg * p.qh + h_loc) * D + lane * kPer;
     const float inv = 1.f / L;
 #pragma unroll
-    for (int t = 0; t < kPer; ++t) dst[lane + 32 * t] = __float2bfloat16_rn(acc[t] * inv);
+    for (int u = 0; u < kPer; u += 2)
+        *reinterpret_cast<uint32_t *>(dst + u) = pack_bf16x2(acc[u] * inv, acc[u + 1] * inv);
 }
 
 // ------------------------------------------------------------------ host side
@@ -549,6 +579,24 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
     return w;
 }
 
+// Launch as a programmatic dependent of the previous kernel in the stream:
+// the kernel calls griddepcontrol.wait before it reads that kernel's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D>
 cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtensorMap &mk,
                         const CUtensorMap &mv, int grid, cudaStream_t stream, bool timed) {
@@ -559,13 +607,12 @@ cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtens
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (timed) timing_begin(stream);
-    kern<<<grid, 32 * (prm.kvh + 1), smem, stream>>>(mk, mv, prm);
+    e = launch_dependent(kern, dim3(grid), dim3(32 * (prm.kvh + 1)), smem, stream, mk, mv, prm);
     if (timed) timing_end(stream);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int warps = prm.nhg * prm.num_seqs * prm.qh;
-    split_decode_reduce_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(prm, grid);
-    return cudaGetLastError();
+    return launch_dependent(split_decode_reduce_kernel<D>, dim3((warps + 7) / 8), dim3(256), 0, stream,
+                            prm, grid);
 }
 
 int stages_for(int kvh, int qh, int D) {
@@ -642,11 +689,10 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
     if (plan_grid > 2 * sms) plan_grid = 2 * sms;
     if (plan_grid < 1) plan_grid = 1;
-    decode_plan_kernel<<<plan_grid, kPlanThreads, plan_smem, stream>>>(
-        a.context_lens, a.cu_seqlens_q, a.block_tables, a.num_seqs, a.max_blocks, a.num_blocks,
-        a.total_q, reinterpret_cast<int32_t *>(ws + w.prefix), reinterpret_cast<StreamEntry *>(ws + w.stream),
-        a.status);
-    e = cudaGetLastError();
+    e = launch_dependent(decode_plan_kernel, dim3(plan_grid), dim3(kPlanThreads), plan_smem, stream,
+                         a.context_lens, a.cu_seqlens_q, a.block_tables, a.num_seqs, a.max_blocks,
+                         a.num_blocks, a.total_q, reinterpret_cast<int32_t *>(ws + w.prefix),
+                         reinterpret_cast<StreamEntry *>(ws + w.stream), a.status);
     if (e != cudaSuccess) return e;
 
     int grid = sms;
