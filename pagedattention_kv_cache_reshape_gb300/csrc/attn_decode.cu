@@ -84,13 +84,6 @@ struct DecodeParams {
     int32_t *status;
 };
 
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependents_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ------------------------------------------------------------------ plan
 __global__ void __launch_bounds__(kPlanThreads)
     decode_plan_kernel(const int32_t *__restrict__ context_lens,
@@ -577,24 +570,6 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
     w.part_o = align_up(w.part_ml + sizeof(float) * 2 * slots_heads, 256);
     w.total = align_up(w.part_o + sizeof(float) * (size_t)head_dim * slots_heads, 256);
     return w;
-}
-
-// Launch as a programmatic dependent of the previous kernel in the stream:
-// the kernel calls griddepcontrol.wait before it reads that kernel's output.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t stream, Args &&...args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 template <int D>

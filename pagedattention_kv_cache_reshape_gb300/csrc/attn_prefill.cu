@@ -12,7 +12,8 @@
 //
 // Work unit (one CTA): 128 rows = POS consecutive query positions x the G
 // query heads of one kv-head (so each K/V tile is loaded once for the whole
-// group), against the sequence's keys in tiles of 128 (8 cache blocks).
+// group), against the sequence's keys in tiles of 64 (4 cache blocks); two
+// CTAs share an SM so two softmax warpgroups overlap each other's MMAs.
 // Warp roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
 // warp 4 TMA producer, warp 5 TMEM owner and MMA issuer (one thread).
 //   S_j = Q K_j^T   -> TMEM (two buffers, so S_{j+1} overlaps softmax j)
@@ -36,13 +37,13 @@ namespace {
 
 constexpr int kB = kBlockSize;
 constexpr int BM = 128;               // rows per tile
-constexpr int BN = 128;               // keys per KV tile
+constexpr int BN = 64;                // keys per KV tile (4 cache blocks)
 constexpr int kBlocksPerTile = BN / kB;
 constexpr int kThreads = 192;
 constexpr int kPlanThreads = 512;
-constexpr int kTmemCols = 512;
-constexpr uint32_t kSColStride = 128;  // S buffer b at TMEM column b * 128
-constexpr uint32_t kOCol = 256;
+constexpr int kTmemCols = 256;        // two CTAs share an SM's 512 columns
+constexpr uint32_t kSColStride = BN;  // S buffer b at TMEM column b * BN
+constexpr uint32_t kOCol = 2 * BN;    // O after the two S buffers
 
 struct PrefillParams {
     const int32_t *cu_seqlens_q;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 
 // ------------------------------------------------------------------ main kernel
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
@@ -116,22 +117,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdescQK = umma_idesc_bf16(BM, BN, 0);
     constexpr uint32_t kIdescPV = umma_idesc_bf16(BM, D, 1);
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // all shared state is dynamic (no static shared memory), so the 1024-byte
+    // aligned operand tiles start at offset 0 and two CTAs fit on one SM
+    extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *q_s = smem;
     uint8_t *k_s0 = smem + kQBytes;
     uint8_t *v_s0 = smem + kQBytes + 2 * kKVBytes;
     uint8_t *p_s = smem + kQBytes + 4 * kKVBytes;
-    __shared__ __align__(8) uint64_t bars[9];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(p_s + BM * BN * 2);
     uint64_t *q_full = bars + 0;
     uint64_t *kv_full = bars + 1;   // [2]
     uint64_t *kv_empty = bars + 3;  // [2]
     uint64_t *s_full = bars + 5;    // [2]
     uint64_t *p_full = bars + 7;
     uint64_t *o_done = bars + 8;
-    __shared__ uint32_t tmem_base_s;
-    __shared__ int abort_flag;
+    uint32_t &tmem_base_s = *reinterpret_cast<uint32_t *>(bars + 9);
+    int &abort_flag = *(reinterpret_cast<int *>(bars + 9) + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.y;
@@ -154,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos_last = pos_base + nrows - 1;
     const int nkv = pos_last / BN + 1;
     const int nb = (ctx + kB - 1) / kB;
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
+        if (tid == 0) set_status(p.status, PA_ERR_CUDA);
+        return;
+    }
 
     if (tid == 0) {
         mbar_init(q_full, 1);
@@ -183,37 +188,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(q_full, kQBytes);
             tma_load_4d(q_s, &tmap_q, 0, q0 + i0, g * p.group, 0, q_full);
         }
+        // block ids, 32 per chunk (lane l holds block 32*chunk + l), one chunk ahead;
+        // past the sequence end (or invalid) the coordinate num_blocks is out of
+        // bounds and TMA fills zeros
         const int32_t *bt = p.block_tables + (int64_t)s * p.max_blocks;
-        for (int j = 0; j < nkv; ++j) {
-            const int stage = j & 1;
-            if (lane == 0 && j >= 2 && !mbar_wait(kv_empty + stage, ((j >> 1) - 1) & 1)) ok = false;
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            // physical blocks of this tile; past the sequence end (or invalid)
-            // the coordinate num_blocks is out of bounds and TMA fills zeros
+        auto load_ids = [&](int chunk) {
+            const int lb = chunk * 32 + lane;
             int coord = p.num_blocks;
-            const int lb = j * kBlocksPerTile + lane;
-            if (lane < kBlocksPerTile && lb < nb) {
+            if (lb < nb) {
                 const int32_t blk = __ldg(bt + lb);
                 if (blk >= 0 && blk < p.num_blocks) coord = blk;
                 else set_status(p.status, PA_ERR_OUT_OF_RANGE);
             }
+            return coord;
+        };
+        int ids_cur = load_ids(0), ids_next = load_ids(1), chunk_cur = 0;
+        for (int j = 0; j < nkv; ++j) {
+            const int stage = j & 1;
+            if ((j * kBlocksPerTile) / 32 != chunk_cur) {   // move to the next chunk
+                ids_cur = ids_next;
+                ++chunk_cur;
+                ids_next = load_ids(chunk_cur + 1);
+            }
+            if (lane == 0 && j >= 2 && !mbar_wait(kv_empty + stage, ((j >> 1) - 1) & 1)) ok = false;
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
             int coords[kBlocksPerTile];
+            const int lb0 = (j * kBlocksPerTile) & 31;
 #pragma unroll
-            for (int b = 0; b < kBlocksPerTile; ++b) coords[b] = __shfl_sync(0xffffffffu, coord, b);
-            if (lane == 0) {
-                uint8_t *ks = k_s0 + stage * kKVBytes;
-                uint8_t *vs = v_s0 + stage * kKVBytes;
-                mbar_arrive_expect_tx(kv_full + stage, 2 * kKVBytes);
+            for (int b = 0; b < kBlocksPerTile; ++b) coords[b] = __shfl_sync(0xffffffffu, ids_cur, lb0 + b);
+            // lane 0 arms the barrier, then lanes (block, plane) issue one K and one V copy each
+            if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, 2 * kKVBytes);
+            __syncwarp();
+            if (lane < kBlocksPerTile * kDH) {
+                const int b = lane / kDH, dh = lane % kDH;
+                int cb = coords[0];
 #pragma unroll
-                for (int b = 0; b < kBlocksPerTile; ++b)
-#pragma unroll
-                    for (int dh = 0; dh < kDH; ++dh) {
-                        tma_load_5d(ks + dh * kPlaneKV + b * (kB * 128), &tmap_k, 0, 0, dh, g, coords[b],
-                                    kv_full + stage);
-                        tma_load_5d(vs + dh * kPlaneKV + b * (kB * 128), &tmap_v, 0, 0, dh, g, coords[b],
-                                    kv_full + stage);
-                    }
+                for (int u = 1; u < kBlocksPerTile; ++u) cb = b == u ? coords[u] : cb;
+                const uint32_t off = dh * kPlaneKV + b * (kB * 128);
+                tma_load_5d(k_s0 + stage * kKVBytes + off, &tmap_k, 0, 0, dh, g, cb, kv_full + stage);
+                tma_load_5d(v_s0 + stage * kKVBytes + off, &tmap_v, 0, 0, dh, g, cb, kv_full + stage);
             }
         }
         if (!ok && lane == 0) {
@@ -310,13 +324,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mx = fmaxf(mx, v);
                 }
             const float m_new = fmaxf(m, mx);
-            const bool need = m_new > m + 8.f;
+            // the running max moves only when it grows by more than 2^8
+            const bool need = (j == 0) || m_new > m + 8.f;
+            const float m_use_new = need ? m_new : m;
+            const float m_use = m_use_new == -INFINITY ? 0.f : m_use_new;
+            // P = exp2(S - m) in registers, before waiting for the previous P*V
+            float lsum = 0.f;
+            uint32_t pw[BN / 2];
+#pragma unroll
+            for (int u = 0; u < BN / 2; ++u) {
+                const float p0 = fast_exp2(sv[2 * u] - m_use);
+                const float p1 = fast_exp2(sv[2 * u + 1] - m_use);
+                lsum += p0 + p1;
+                pw[u] = pack_bf16x2(p0, p1);
+            }
             if (j > 0) {
                 if (!mbar_wait(o_done, (j - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, need)) {
                     const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-                    if (need) m = m_new;
                     l *= alpha;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -329,10 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                 }
-            } else {
-                m = m_new;
             }
-            const float m_use = m == -INFINITY ? 0.f : m;
+            m = m_use_new;
             // value rows past the context end inside the last block -> zero
             if (t_tail != 0) {
                 const int b = lb_last - j * kBlocksPerTile;
@@ -350,25 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // P = exp2(S - m) as bf16, K-major 128-byte swizzled rows
-            float lsum = 0.f;
+            // P as bf16, K-major 128-byte swizzled rows
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t w[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float p0 = fast_exp2(sv[32 * c + 2 * u] - m_use);
-                    const float p1 = fast_exp2(sv[32 * c + 2 * u + 1] - m_use);
-                    lsum += p0 + p1;
-                    w[u] = pack_bf16x2(p0, p1);
-                }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int kt = 32 * c + 8 * q4;                 // first key of this 16-byte chunk
-                    const int chunk = (kt & 63) >> 3;
-                    uint8_t *dst = p_s + (kt >> 6) * kPlaneQ + r * 128 + ((chunk ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-                }
+            for (int q4 = 0; q4 < BN / 8; ++q4) {
+                const int kt = 8 * q4;                          // first key of this 16-byte chunk
+                const int chunk = (kt & 63) >> 3;
+                uint8_t *dst = p_s + (kt >> 6) * kPlaneQ + r * 128 + ((chunk ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
             }
             l += lsum;
             fence_proxy_async_smem();
@@ -452,9 +464,12 @@ int log2_exact(int v) {
 template <int D>
 cudaError_t launch_main(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                         const PrefillParams &prm, int grid_x, int num_kv_heads, cudaStream_t stream) {
-    const size_t smem = 1024 + (size_t)BM * D * 2 + 4 * (size_t)BN * D * 2 + (size_t)BM * BN * 2;
+    const size_t smem = (size_t)BM * D * 2 + 4 * (size_t)BN * D * 2 + (size_t)BM * BN * 2 + 128;
     auto kern = prefill_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     kern<<<dim3(grid_x, num_kv_heads), kThreads, smem, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError();

@@ -19,6 +19,8 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_tables, in
                                     const int32_t *__restrict__ cu_seqlens_q, int total_new,
                                     int block_size, int num_blocks,
                                     int64_t *__restrict__ slot_mapping, int32_t *status) {
+    grid_dependency_wait();      // inputs may come from the previous kernel
+    grid_dependents_launch();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= total_new) return;
     int lo = 0, hi = num_seqs;  // find the last s with cu[s] <= t
@@ -50,6 +52,8 @@ __global__ void reshape_and_cache_kernel(const char *__restrict__ key,
                                          const int64_t *__restrict__ slot_mapping,
                                          int num_tokens, int row_vecs, int64_t pool_slots,
                                          int32_t *status) {
+    grid_dependency_wait();      // the slot mapping may come from the previous kernel
+    grid_dependents_launch();
     const int warps = blockDim.x >> 5;
     const int t = blockIdx.x * warps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -81,11 +85,9 @@ cudaError_t launch_slot_mapping(const int32_t *block_tables, int num_seqs, int m
     if (total_new == 0) return cudaSuccess;
     const int threads = 256;
     const int grid = (total_new + threads - 1) / threads;
-    slot_mapping_kernel<<<grid, threads, 0, stream>>>(block_tables, num_seqs, max_blocks,
-                                                      seq_start, cu_seqlens_q, total_new,
-                                                      block_size, num_blocks, slot_mapping,
-                                                      status);
-    return cudaGetLastError();
+    return launch_dependent(slot_mapping_kernel, dim3(grid), dim3(threads), 0, stream, block_tables,
+                            num_seqs, max_blocks, seq_start, cu_seqlens_q, total_new, block_size,
+                            num_blocks, slot_mapping, status);
 }
 
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t key_stride,
@@ -103,25 +105,20 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
     const int threads = 256, warps = threads / 32;
     const int grid = (num_tokens + warps - 1) / warps;
     const int64_t pool_slots = (int64_t)num_blocks * block_size;
-    if (v16) {
-        reshape_and_cache_kernel<uint4><<<grid, threads, 0, stream>>>(
-            (const char *)key, (const char *)value, ks, vs, (char *)k_cache, (char *)v_cache,
-            slot_mapping, num_tokens, (int)(row_bytes / 16), pool_slots, status);
-    } else {
-        // element-sized copies (rows are whole elements: 2 or 4 bytes)
-        if (elem_bytes == 4) {
-            reshape_and_cache_kernel<uint32_t><<<grid, threads, 0, stream>>>(
-                (const char *)key, (const char *)value, ks, vs, (char *)k_cache,
-                (char *)v_cache, slot_mapping, num_tokens, (int)(row_bytes / 4), pool_slots,
-                status);
-        } else {
-            reshape_and_cache_kernel<uint16_t><<<grid, threads, 0, stream>>>(
-                (const char *)key, (const char *)value, ks, vs, (char *)k_cache,
-                (char *)v_cache, slot_mapping, num_tokens, (int)(row_bytes / 2), pool_slots,
-                status);
-        }
-    }
-    return cudaGetLastError();
+    const char *kp = static_cast<const char *>(key), *vp = static_cast<const char *>(value);
+    char *kc = static_cast<char *>(k_cache), *vc = static_cast<char *>(v_cache);
+    if (v16)
+        return launch_dependent(reshape_and_cache_kernel<uint4>, dim3(grid), dim3(threads), 0, stream,
+                                kp, vp, ks, vs, kc, vc, slot_mapping, num_tokens, (int)(row_bytes / 16),
+                                pool_slots, status);
+    // element-sized copies (rows are whole elements: 2 or 4 bytes)
+    if (elem_bytes == 4)
+        return launch_dependent(reshape_and_cache_kernel<uint32_t>, dim3(grid), dim3(threads), 0, stream,
+                                kp, vp, ks, vs, kc, vc, slot_mapping, num_tokens, (int)(row_bytes / 4),
+                                pool_slots, status);
+    return launch_dependent(reshape_and_cache_kernel<uint16_t>, dim3(grid), dim3(threads), 0, stream,
+                            kp, vp, ks, vs, kc, vc, slot_mapping, num_tokens, (int)(row_bytes / 2),
+                            pool_slots, status);
 }
 
 }  // namespace pa

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pa.h"
 
 namespace pa {
@@ -79,5 +81,24 @@ bool prefill_tc_supported(const AttnArgs &a);
 size_t prefill_workspace(int num_seqs, int total_q);
 cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspace_bytes,
                               cudaStream_t stream);
+
+// Launch as a programmatic dependent of the previous kernel in the stream:
+// the kernel calls griddepcontrol.wait before it reads that kernel's output.
+template <typename... KArgs, typename... Args>
+inline
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 }  // namespace pa
