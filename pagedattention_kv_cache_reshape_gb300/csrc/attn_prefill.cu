@@ -10,15 +10,17 @@
 // ctx - q_len + i) and q-head h,
 //     out[row][h] = sum_{j <= pos} softmax_j(scale * <q[row][h], K_s[j][g(h)]>) V_s[j][g(h)].
 //
-// Work unit (one CTA): 128 rows = POS consecutive query positions x the G
-// query heads of one kv-head (so each K/V tile is loaded once for the whole
-// group), against the sequence's keys in tiles of 64 (4 cache blocks); two
-// CTAs share an SM so two softmax warpgroups overlap each other's MMAs.
-// Warp roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
-// warp 4 TMA producer, warp 5 TMEM owner and MMA issuer (one thread).
-//   S_j = Q K_j^T   -> TMEM (two buffers, so S_{j+1} overlaps softmax j)
-//   P_j = exp2(S_j * scale*log2e - m)  (bf16, shared memory, K-major)
-//   O  += P_j V_j   -> TMEM (fp32)
+// Work unit (one CTA): two M-tiles of 128 rows; a tile is POS consecutive
+// query positions x the G query heads of one kv-head, so each K/V tile is
+// loaded once for 2*POS positions of the whole group.  Keys come in tiles of
+// 64 (4 cache blocks) through a 3-deep TMA ring.
+// Warp roles: warps 0-7 two softmax warpgroups (thread = row = TMEM lane of
+// its tile), warp 8 TMA producer, warp 9 TMEM owner and MMA issuer.
+//   S_t,j = Q_t K_j^T  -> TMEM (two buffers per tile)
+//   P_t,j = exp2(S_t,j * scale*log2e - m)  (bf16, shared memory, two buffers)
+//   O_t  += P_t,j V_j  -> TMEM (fp32)
+// The issuer runs QK of KV tile j for both M-tiles before PV of tile j-1, so
+// the tensor pipe has work while the softmax warpgroups turn S into P.
 // The running max is only raised (and O rescaled in TMEM) when a row's max
 // grows by more than 2^8; otherwise the stale max is kept, which changes no
 // result because l uses the same max.  Causal masking is a select on the
@@ -36,14 +38,16 @@ namespace pa {
 namespace {
 
 constexpr int kB = kBlockSize;
-constexpr int BM = 128;               // rows per tile
+constexpr int BM = 128;               // rows per M-tile
+constexpr int kMT = 2;                // M-tiles per CTA, one softmax warpgroup each
 constexpr int BN = 64;                // keys per KV tile (4 cache blocks)
+constexpr int kStages = 3;            // K/V ring depth
 constexpr int kBlocksPerTile = BN / kB;
-constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4 * kMT;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kPlanThreads = 512;
-constexpr int kTmemCols = 256;        // two CTAs share an SM's 512 columns
-constexpr uint32_t kSColStride = BN;  // S buffer b at TMEM column b * BN
-constexpr uint32_t kOCol = 2 * BN;    // O after the two S buffers
+constexpr int kTmemCols = 512;
 
 struct PrefillParams {
     const int32_t *cu_seqlens_q;
@@ -105,34 +109,35 @@ __global__ void __launch_bounds__(kPlanThreads)
 
 // ------------------------------------------------------------------ main kernel
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
     constexpr int kDH = D / 64;             // 64-column planes of a head
-    constexpr int kQBytes = BM * D * 2;
-    constexpr int kKVBytes = BN * D * 2;    // K (or V) of one tile
+    constexpr int kQBytes = BM * D * 2;     // one M-tile of Q
+    constexpr int kKVBytes = BN * D * 2;    // K (or V) of one KV tile
+    constexpr int kPBytes = BM * BN * 2;    // one P buffer
     constexpr int kPlaneQ = BM * 128;       // one 64-column plane of Q or P
     constexpr int kPlaneKV = BN * 128;      // one 64-column plane of K or V
     constexpr uint32_t kIdescQK = umma_idesc_bf16(BM, BN, 0);
     constexpr uint32_t kIdescPV = umma_idesc_bf16(BM, D, 1);
 
-    // all shared state is dynamic (no static shared memory), so the 1024-byte
-    // aligned operand tiles start at offset 0 and two CTAs fit on one SM
+    // all shared state is dynamic so the 1024-byte aligned tiles start at 0:
+    // Q[2] | (K,V) x kStages | P[2 tiles][2 buffers] | barriers
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *q_s = smem;
-    uint8_t *k_s0 = smem + kQBytes;
-    uint8_t *v_s0 = smem + kQBytes + 2 * kKVBytes;
-    uint8_t *p_s = smem + kQBytes + 4 * kKVBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(p_s + BM * BN * 2);
-    uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;   // [2]
-    uint64_t *kv_empty = bars + 3;  // [2]
-    uint64_t *s_full = bars + 5;    // [2]
-    uint64_t *p_full = bars + 7;
-    uint64_t *o_done = bars + 8;
-    uint32_t &tmem_base_s = *reinterpret_cast<uint32_t *>(bars + 9);
-    int &abort_flag = *(reinterpret_cast<int *>(bars + 9) + 1);
+    uint8_t *kv_s = smem + kMT * kQBytes;
+    uint8_t *p_s = kv_s + kStages * 2 * kKVBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(p_s + kMT * 2 * kPBytes);
+    uint64_t *q_full = bars;                       // 1
+    uint64_t *kv_full = q_full + 1;                // [kStages]
+    uint64_t *kv_empty = kv_full + kStages;        // [kStages]
+    uint64_t *s_full = kv_empty + kStages;         // [tile][buf]
+    uint64_t *p_full = s_full + 4;                 // [tile][buf]
+    uint64_t *p_free = p_full + 4;                 // [tile][buf]
+    uint64_t *drained = p_free + 4;                // 1: every product issued has completed
+    uint32_t &tmem_base_s = *reinterpret_cast<uint32_t *>(drained + 1);
+    int &abort_flag = *(reinterpret_cast<int *>(drained + 1) + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.y;
@@ -147,12 +152,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (tid == 0) set_status(p.status, PA_ERR_OUT_OF_RANGE);
         return;
     }
-    const int POS = 1 << p.pos_shift;
-    const int i0 = tile * POS;
-    const int nrows = min(POS, q_len - i0);
-    if (nrows <= 0) return;
+    const int POS = 1 << p.pos_shift;                  // query positions per M-tile
+    const int i0 = tile * kMT * POS;                   // first position of M-tile 0
+    const int nrows_all = min(kMT * POS, q_len - i0);  // valid positions of the CTA
+    if (nrows_all <= 0) return;
     const int pos_base = ctx - q_len + i0;
-    const int pos_last = pos_base + nrows - 1;
+    const int pos_last = pos_base + nrows_all - 1;
     const int nkv = pos_last / BN + 1;
     const int nb = (ctx + kB - 1) / kB;
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
@@ -162,31 +167,38 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (tid == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(kv_full + i, 1);
             mbar_init(kv_empty + i, 1);
-            mbar_init(s_full + i, 1);
         }
-        mbar_init(p_full, BM);
-        mbar_init(o_done, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(s_full + i, 1);
+            mbar_init(p_full + i, BM);
+            mbar_init(p_free + i, 1);
+        }
+        mbar_init(drained, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(&tmem_base_s, kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(&tmem_base_s, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
+    // TMEM columns: S[tile][buf] at (2 tile + buf) * BN, O[tile] at 4 BN + tile * D
+    auto s_col = [](int t, int b) { return (uint32_t)((2 * t + b) * BN); };
+    auto o_col = [](int t) { return (uint32_t)(4 * BN + t * D); };
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ================= TMA producer
         bool ok = true;
         if (lane == 0) {
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            mbar_arrive_expect_tx(q_full, kQBytes);
-            tma_load_4d(q_s, &tmap_q, 0, q0 + i0, g * p.group, 0, q_full);
+            mbar_arrive_expect_tx(q_full, kMT * kQBytes);
+            for (int t = 0; t < kMT; ++t)
+                tma_load_4d(q_s + t * kQBytes, &tmap_q, 0, q0 + i0 + t * POS, g * p.group, 0, q_full);
         }
         // block ids, 32 per chunk (lane l holds block 32*chunk + l), one chunk ahead;
         // past the sequence end (or invalid) the coordinate num_blocks is out of
@@ -204,13 +216,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         };
         int ids_cur = load_ids(0), ids_next = load_ids(1), chunk_cur = 0;
         for (int j = 0; j < nkv; ++j) {
-            const int stage = j & 1;
-            if ((j * kBlocksPerTile) / 32 != chunk_cur) {   // move to the next chunk
+            const int stage = j % kStages;
+            if ((j * kBlocksPerTile) / 32 != chunk_cur) {
                 ids_cur = ids_next;
                 ++chunk_cur;
                 ids_next = load_ids(chunk_cur + 1);
             }
-            if (lane == 0 && j >= 2 && !mbar_wait(kv_empty + stage, ((j >> 1) - 1) & 1)) ok = false;
+            if (lane == 0 && j >= kStages && !mbar_wait(kv_empty + stage, ((j / kStages) - 1) & 1)) ok = false;
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
             int coords[kBlocksPerTile];
@@ -226,8 +238,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int u = 1; u < kBlocksPerTile; ++u) cb = b == u ? coords[u] : cb;
                 const uint32_t off = dh * kPlaneKV + b * (kB * 128);
-                tma_load_5d(k_s0 + stage * kKVBytes + off, &tmap_k, 0, 0, dh, g, cb, kv_full + stage);
-                tma_load_5d(v_s0 + stage * kKVBytes + off, &tmap_v, 0, 0, dh, g, cb, kv_full + stage);
+                uint8_t *ks = kv_s + stage * 2 * kKVBytes;
+                tma_load_5d(ks + off, &tmap_k, 0, 0, dh, g, cb, kv_full + stage);
+                tma_load_5d(ks + kKVBytes + off, &tmap_v, 0, 0, dh, g, cb, kv_full + stage);
             }
         }
         if (!ok && lane == 0) {
@@ -237,89 +250,105 @@ __global__ void __launch_bounds__(kThreads, 2)
         // every copy this CTA issued has landed before the CTA may exit
         if (lane == 0) {
             mbar_wait(q_full, 0);
-            for (int j = nkv > 2 ? nkv - 2 : 0; j < nkv; ++j) mbar_wait(kv_full + (j & 1), (j >> 1) & 1);
+            for (int j = nkv > kStages ? nkv - kStages : 0; j < nkv; ++j)
+                mbar_wait(kv_full + (j % kStages), (j / kStages) & 1);
         }
-    } else if (warp == 5) {
-        // ================= MMA issuer (one thread)
+    } else if (warp == kMmaWarp) {
+        // ================= MMA issuer (one thread): QK of KV tile j for both
+        // M-tiles, then PV of tile j-1, so the tensor pipe has work while the
+        // softmax warpgroups turn S into P
         if (lane == 0) {
-            const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
-            auto issue_qk = [&](int j) {
-                const uint32_t k_addr = smem_u32(k_s0 + (j & 1) * kKVBytes);
+            const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s), kv_addr = smem_u32(kv_s);
+            auto issue_qk = [&](int t, int j) {
+                const uint32_t k_addr = kv_addr + (j % kStages) * 2 * kKVBytes;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off_q = (ks >> 2) * kPlaneQ + (ks & 3) * 32;
+                    const uint32_t off_q = t * kQBytes + (ks >> 2) * kPlaneQ + (ks & 3) * 32;
                     const uint32_t off_k = (ks >> 2) * kPlaneKV + (ks & 3) * 32;
-                    umma_bf16(tmem + (uint32_t)(j & 1) * kSColStride, umma_desc_sw128(q_addr + off_q, 16, 1024),
+                    umma_bf16(tmem + s_col(t, j & 1), umma_desc_sw128(q_addr + off_q, 16, 1024),
                               umma_desc_sw128(k_addr + off_k, 16, 1024), kIdescQK, ks > 0);
                 }
             };
-            auto issue_pv = [&](int j) {
-                const uint32_t v_addr = smem_u32(v_s0 + (j & 1) * kKVBytes);
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t v_addr = kv_addr + (j % kStages) * 2 * kKVBytes + kKVBytes;
+                const uint32_t pb = p_addr + (2 * t + (j & 1)) * kPBytes;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint32_t off_p = (kk >> 2) * kPlaneQ + (kk & 3) * 32;
-                    umma_bf16(tmem + kOCol, umma_desc_sw128(p_addr + off_p, 16, 1024),
+                    umma_bf16(tmem + o_col(t), umma_desc_sw128(pb + off_p, 16, 1024),
                               umma_desc_sw128(v_addr + kk * 2048, kPlaneKV, 1024), kIdescPV,
                               (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(q_full, 0) && mbar_wait(kv_full, 0);
-            if (ok) {
-                tc_fence_after();
-                issue_qk(0);
-                umma_commit(s_full);
-            }
-            int issued_pv = 0;
-            for (int j = 0; ok && j < nkv; ++j) {
-                if (j + 1 < nkv) {
-                    if (!mbar_wait(kv_full + ((j + 1) & 1), ((j + 1) >> 1) & 1)) { ok = false; break; }
+            auto pv_step = [&](int j) -> bool {   // PV of KV tile j for both M-tiles
+                for (int t = 0; t < kMT; ++t) {
+                    if (!mbar_wait(p_full + 2 * t + (j & 1), (j >> 1) & 1)) return false;
                     tc_fence_after();
-                    issue_qk(j + 1);
-                    umma_commit(s_full + ((j + 1) & 1));
+                    issue_pv(t, j);
+                    umma_commit(p_free + 2 * t + (j & 1));
                 }
-                if (!mbar_wait(p_full, j & 1)) { ok = false; break; }
+                umma_commit(kv_empty + (j % kStages));
+                return true;
+            };
+            bool ok = mbar_wait(q_full, 0);
+            int pv_issued = 0;
+            for (int j = 0; ok && j < nkv; ++j) {
+                if (!mbar_wait(kv_full + (j % kStages), (j / kStages) & 1)) { ok = false; break; }
                 tc_fence_after();
-                issue_pv(j);
-                umma_commit(o_done);
-                umma_commit(kv_empty + (j & 1));
-                ++issued_pv;
+                for (int t = 0; t < kMT; ++t) {
+                    issue_qk(t, j);
+                    umma_commit(s_full + 2 * t + (j & 1));
+                }
+                if (j >= 1) {
+                    if (!pv_step(j - 1)) { ok = false; break; }
+                    ++pv_issued;
+                }
+            }
+            if (ok) {
+                if (pv_step(nkv - 1)) ++pv_issued;
+                else ok = false;
             }
             if (!ok) {
                 set_status(p.status, PA_ERR_TIMEOUT);
                 abort_flag = 1;
             }
-            // drain: the last product must finish before TMEM is released
-            if (issued_pv > 0) mbar_wait(o_done, (issued_pv - 1) & 1);
+            // drain: everything issued must finish before TMEM is released
+            umma_commit(drained);
+            mbar_wait(drained, 0);
+            (void)pv_issued;
         }
         __syncwarp();
     } else {
-        // ================= softmax warpgroup: thread r owns row r (TMEM lane r)
-        const int r = tid;
+        // ================= softmax warpgroup t: thread r owns row r of M-tile t
+        const int t = warp >> 2;
+        const int r = tid & (BM - 1);
         const int h_local = r >> p.pos_shift;
-        const int i = r & (POS - 1);
-        const bool row_valid = i < nrows;
-        const int pos = pos_base + (row_valid ? i : nrows - 1);
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        const int i = t * POS + (r & (POS - 1));          // position index within the CTA
+        const bool row_valid = i < nrows_all;
+        const int pos = pos_base + (row_valid ? i : nrows_all - 1);
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int t_tail = ctx & (kB - 1);          // valid tokens in the last block (0 = full)
         const int lb_last = (ctx - 1) / kB;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            if (!mbar_wait(s_full + (j & 1), (j >> 1) & 1)) { ok = false; break; }
+            const int b = j & 1;
+            if (!mbar_wait(s_full + 2 * t + b, (j >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
             uint32_t raw[BN / 32][32];
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_addr + (uint32_t)(j & 1) * kSColStride + 32 * c, raw[c]);
+            for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_addr + s_col(t, b) + 32 * c, raw[c]);
             tmem_wait_ld();
             float sv[BN];
             float mx = -INFINITY;
             const int key0 = j * BN;
+            const bool diag = key0 + BN - 1 > pos_base + t * POS;   // a key past some row of this tile
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int key = key0 + 32 * c + e;
-                    const float v = key <= pos ? __uint_as_float(raw[c][e]) * p.scale_log2 : -INFINITY;
+                    const float x = __uint_as_float(raw[c][e]) * p.scale_log2;
+                    const float v = (!diag || key0 + 32 * c + e <= pos) ? x : -INFINITY;
                     sv[32 * c + e] = v;
                     mx = fmaxf(mx, v);
                 }
@@ -328,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool need = (j == 0) || m_new > m + 8.f;
             const float m_use_new = need ? m_new : m;
             const float m_use = m_use_new == -INFINITY ? 0.f : m_use_new;
-            // P = exp2(S - m) in registers, before waiting for the previous P*V
             float lsum = 0.f;
             uint32_t pw[BN / 2];
 #pragma unroll
@@ -338,57 +366,63 @@ __global__ void __launch_bounds__(kThreads, 2)
                 lsum += p0 + p1;
                 pw[u] = pack_bf16x2(p0, p1);
             }
-            if (j > 0) {
-                if (!mbar_wait(o_done, (j - 1) & 1)) { ok = false; break; }
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // O must hold every earlier product before it is rescaled: wait
+                // for the commit of PV(j-1) on its P buffer (that barrier is at
+                // most one phase ahead of this wait, so its parity is exact;
+                // a commit also covers every earlier product)
+                if (!mbar_wait(p_free + 2 * t + ((j - 1) & 1), ((j - 1) >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-                    l *= alpha;
+                const float alpha = need ? fast_exp2(m - m_new) : 1.f;
+                l *= alpha;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_addr + kOCol + 32 * c, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(lane_addr + kOCol + 32 * c, o);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(lane_addr + o_col(t) + 32 * c, o);
                 }
+                tmem_wait_st();
             }
             m = m_use_new;
             // value rows past the context end inside the last block -> zero
-            if (t_tail != 0) {
-                const int b = lb_last - j * kBlocksPerTile;
-                if (b >= 0 && b < kBlocksPerTile) {
-                    if (!mbar_wait(kv_full + (j & 1), (j >> 1) & 1)) { ok = false; break; }
-                    uint8_t *vs = v_s0 + (j & 1) * kKVBytes;
+            // (warpgroup 0 only; its p_full arrival orders the writes before
+            // every product of this KV tile)
+            if (t == 0 && t_tail != 0) {
+                const int bb = lb_last - j * kBlocksPerTile;
+                if (bb >= 0 && bb < kBlocksPerTile) {
+                    if (!mbar_wait(kv_full + (j % kStages), (j / kStages) & 1)) { ok = false; break; }
+                    uint8_t *vs = kv_s + (j % kStages) * 2 * kKVBytes + kKVBytes;
                     const int rows_zero = kB - t_tail;
                     const int n16 = kDH * rows_zero * 8;
                     for (int u = r; u < n16; u += BM) {
                         const int dh = u / (rows_zero * 8);
                         const int rem = u - dh * rows_zero * 8;
                         const int tok = t_tail + (rem >> 3);
-                        *reinterpret_cast<uint4 *>(vs + dh * kPlaneKV + (b * kB + tok) * 128 + (rem & 7) * 16) =
+                        *reinterpret_cast<uint4 *>(vs + dh * kPlaneKV + (bb * kB + tok) * 128 + (rem & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
             }
-            // P as bf16, K-major 128-byte swizzled rows
+            // the P buffer is free once the product two tiles back has read it
+            if (j >= 2 && !mbar_wait(p_free + 2 * t + b, ((j >> 1) - 1) & 1)) { ok = false; break; }
+            uint8_t *pbuf = p_s + (2 * t + b) * kPBytes;
 #pragma unroll
             for (int q4 = 0; q4 < BN / 8; ++q4) {
                 const int kt = 8 * q4;                          // first key of this 16-byte chunk
                 const int chunk = (kt & 63) >> 3;
-                uint8_t *dst = p_s + (kt >> 6) * kPlaneQ + r * 128 + ((chunk ^ (r & 7)) << 4);
+                uint8_t *dst = pbuf + (kt >> 6) * kPlaneQ + r * 128 + ((chunk ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
             }
             l += lsum;
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(p_full + 2 * t + b);
         }
-        // ---- epilogue: O / l -> bf16 rows of out
-        if (ok && mbar_wait(o_done, (nkv - 1) & 1)) {
+        // ---- epilogue: O / l -> bf16 rows of out, after the commit of the last product
+        if (ok && mbar_wait(p_free + 2 * t + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1)) {
             tc_fence_after();
             const float inv = 1.f / l;
             __nv_bfloat16 *dst = p.out + ((int64_t)(q0 + i0 + i) * p.num_heads +
@@ -396,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(lane_addr + kOCol + 32 * c, o);
+                tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
                 tmem_wait_ld();
                 if (row_valid) {
 #pragma unroll
@@ -419,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 CUresult make_q_map(CUtensorMap *map, const void *q, int total_q, int num_heads, int D, int pos,
@@ -464,7 +498,8 @@ int log2_exact(int v) {
 template <int D>
 cudaError_t launch_main(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                         const PrefillParams &prm, int grid_x, int num_kv_heads, cudaStream_t stream) {
-    const size_t smem = (size_t)BM * D * 2 + 4 * (size_t)BN * D * 2 + (size_t)BM * BN * 2 + 128;
+    const size_t smem = (size_t)kMT * BM * D * 2 + (size_t)kStages * 2 * BN * D * 2 +
+                        (size_t)kMT * 2 * BM * BN * 2 + 256;
     auto kern = prefill_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -496,7 +531,8 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     const int G = a.num_heads / a.num_kv_heads;
     const int pos = BM / G;
     const int pos_shift = log2_exact(pos);
-    const int capacity = a.total_q / pos + a.num_seqs;
+    const int cta_shift = pos_shift + 1;          // kMT = 2 M-tiles of `pos` positions per CTA
+    const int capacity = a.total_q / (kMT * pos) + a.num_seqs;
     if (workspace_bytes < prefill_workspace(a.num_seqs, a.total_q)) return cudaErrorInvalidValue;
     int32_t *count = static_cast<int32_t *>(workspace);
     int2 *entries = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + 16);
@@ -507,7 +543,7 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
         make_kv_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
 
-    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens_q, a.num_seqs, pos_shift, entries,
+    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens_q, a.num_seqs, cta_shift, entries,
                                                          count, capacity);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
