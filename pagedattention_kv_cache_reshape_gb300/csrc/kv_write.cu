@@ -13,23 +13,31 @@ namespace pa {
 namespace {
 
 // One thread per new token.  The owning sequence is found by binary search
-// over cu_seqlens_q (non-decreasing, cu[0] = 0, cu[num_seqs] = total_new).
+// over cu_seqlens_q (non-decreasing, cu[0] = 0, cu[num_seqs] = total_new),
+// staged in shared memory with one coalesced load when it fits (`staged`).
 __global__ void slot_mapping_kernel(const int32_t *__restrict__ block_tables, int num_seqs,
                                     int max_blocks, const int32_t *__restrict__ seq_start,
                                     const int32_t *__restrict__ cu_seqlens_q, int total_new,
                                     int block_size, int num_blocks,
-                                    int64_t *__restrict__ slot_mapping, int32_t *status) {
+                                    int64_t *__restrict__ slot_mapping, int32_t *status, int staged) {
+    extern __shared__ int32_t cu_s[];
     grid_dependency_wait();      // inputs may come from the previous kernel
     grid_dependents_launch();
+    const int32_t *cu = cu_seqlens_q;
+    if (staged) {
+        for (int i = threadIdx.x; i <= num_seqs; i += blockDim.x) cu_s[i] = __ldg(cu_seqlens_q + i);
+        __syncthreads();
+        cu = cu_s;
+    }
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= total_new) return;
     int lo = 0, hi = num_seqs;  // find the last s with cu[s] <= t
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(cu_seqlens_q + mid) <= t) lo = mid; else hi = mid;
+        if (cu[mid] <= t) lo = mid; else hi = mid;
     }
     const int s = lo;
-    const int64_t pos = (int64_t)__ldg(seq_start + s) + (t - __ldg(cu_seqlens_q + s));
+    const int64_t pos = (int64_t)__ldg(seq_start + s) + (t - cu[s]);
     const int64_t logical = pos / block_size;
     int64_t slot = -1;
     if (pos < 0 || logical >= max_blocks) {
@@ -85,9 +93,11 @@ cudaError_t launch_slot_mapping(const int32_t *block_tables, int num_seqs, int m
     if (total_new == 0) return cudaSuccess;
     const int threads = 256;
     const int grid = (total_new + threads - 1) / threads;
-    return launch_dependent(slot_mapping_kernel, dim3(grid), dim3(threads), 0, stream, block_tables,
-                            num_seqs, max_blocks, seq_start, cu_seqlens_q, total_new, block_size,
-                            num_blocks, slot_mapping, status);
+    const size_t cu_bytes = sizeof(int32_t) * ((size_t)num_seqs + 1);
+    const int staged = cu_bytes <= 32 * 1024 ? 1 : 0;
+    return launch_dependent(slot_mapping_kernel, dim3(grid), dim3(threads), staged ? cu_bytes : 0,
+                            stream, block_tables, num_seqs, max_blocks, seq_start, cu_seqlens_q,
+                            total_new, block_size, num_blocks, slot_mapping, status, staged);
 }
 
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t key_stride,
