@@ -226,18 +226,22 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def step(q=w.q, key=w.key, value=w.value, bt=w.block_tables, ctx=w.context_lens,
-             ss=w.seq_start, cu=w.cu_seqlens_q, o=out):
-        pa.compute_slot_mapping(bt, ss, cu, w.num_blocks, w.total_q, slot_mapping=slots,
-                                dev_status=status, stream=stream)
-        pa.reshape_and_cache(key, value, w.k_cache, w.v_cache, slots, dev_status=status, stream=stream)
+             ss=w.seq_start, cu=w.cu_seqlens_q, o=out, pa_stream=None):
+        pa_stream = stream if pa_stream is None else pa_stream
         if decode_only:
-            pa.decode(q, w.k_cache, w.v_cache, bt, ctx, w.scale, out=o, workspace=workspace,
-                      dev_status=status, stream=stream)
-        else:
-            pa.varlen_prefill(q, cu, w.k_cache, w.v_cache, bt, ctx, w.scale, max_q, out=o,
-                              workspace=workspace, dev_status=status, stream=stream)
+            # slot mapping + cache write + decode through the one-call step entry
+            pa.decode_step(q, key, value, w.k_cache, w.v_cache, bt, ctx, ss, cu, w.scale, out=o,
+                           slot_mapping=slots, workspace=workspace, dev_status=status, stream=pa_stream)
+            return
+        pa.compute_slot_mapping(bt, ss, cu, w.num_blocks, w.total_q, slot_mapping=slots,
+                                dev_status=status, stream=pa_stream)
+        pa.reshape_and_cache(key, value, w.k_cache, w.v_cache, slots, dev_status=status, stream=pa_stream)
+        pa.varlen_prefill(q, cu, w.k_cache, w.v_cache, bt, ctx, w.scale, max_q, out=o,
+                          workspace=workspace, dev_status=status, stream=pa_stream)
 
-    launches_per_step = 2 + 3 + (0 if decode_only else 1)
+    # decode: plan (with the cache write), decode, reduce; mixed: slot mapping,
+    # cache write, plan, decode, reduce, prefill plan, prefill
+    launches_per_step = 3 if decode_only else 7
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -251,25 +255,10 @@ def run_ours(args, world, rank, local):
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            stream_saved = stream
-            pa_stream = side
-
-            def cap_step():
-                pa.compute_slot_mapping(w.block_tables, w.seq_start, w.cu_seqlens_q, w.num_blocks,
-                                        w.total_q, slot_mapping=slots, dev_status=status, stream=pa_stream)
-                pa.reshape_and_cache(w.key, w.value, w.k_cache, w.v_cache, slots, dev_status=status,
-                                     stream=pa_stream)
-                if decode_only:
-                    pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, out=out,
-                              workspace=workspace, dev_status=status, stream=pa_stream)
-                else:
-                    pa.varlen_prefill(w.q, w.cu_seqlens_q, w.k_cache, w.v_cache, w.block_tables,
-                                      w.context_lens, w.scale, max_q, out=out, workspace=workspace,
-                                      dev_status=status, stream=pa_stream)
-            cap_step()
+            step(pa_stream=side)
             side.synchronize()
             with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
-                cap_step()
+                step(pa_stream=side)
         stream.wait_stream(side)
         torch.cuda.synchronize()
         graph = g

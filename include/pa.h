@@ -192,6 +192,31 @@ PA_API pa_status pa_decode_static_scratch(void *out, const void *q, const void *
                                           float scale, pa_dtype dtype, int32_t *dev_status,
                                           pa_stream_t stream);
 
+/*
+ * One decode step in one call: exactly pa_compute_slot_mapping, then
+ * pa_reshape_and_cache of the step's new tokens, then pa_decode (same
+ * arguments, same results; slot_mapping is written as an output).  On the
+ * fast path (bf16, head_dim 64/128, 16-byte aligned rows and strides) the slot
+ * mapping and the cache write run inside the decode plan kernel, saving two
+ * launches and their dependent memory round trips; otherwise the three calls
+ * run one after the other.
+ *  key, value     device [total_new][num_kv_heads][head_dim], token strides given
+ *  seq_start      device int32 [num_seqs]: tokens cached before this step
+ *  cu_seqlens_new device int32 [num_seqs + 1]: offsets of the new tokens
+ *  workspace      >= pa_decode_workspace_size(...) bytes
+ * Each query row s attends to context_lens[s] tokens, which must include the
+ * tokens this call writes.
+ */
+PA_API pa_status pa_decode_step(void *out, const void *q, const void *key, const void *value,
+                                int64_t key_stride_tok, int64_t value_stride_tok, void *k_cache,
+                                void *v_cache, const int32_t *block_tables,
+                                const int32_t *context_lens, const int32_t *seq_start,
+                                const int32_t *cu_seqlens_new, int total_new,
+                                int64_t *slot_mapping, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                                int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream);
+
 /* Workspace bytes pa_varlen_prefill needs for these sizes. */
 PA_API size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
                                         int num_kv_heads, int head_dim, int block_size,

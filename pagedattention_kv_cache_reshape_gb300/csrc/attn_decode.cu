@@ -84,18 +84,77 @@ struct DecodeParams {
     int32_t *status;
 };
 
+// Optional cache write folded into the plan kernel (pa_decode_step): for new
+// token t of sequence s (cu_new[s] <= t < cu_new[s+1]) at position
+// p = seq_start[s] + t - cu_new[s], slot = block_tables[s][p/16]*16 + p%16;
+// the token's K and V rows are copied there with 16-byte vectors.
+struct KvWriteJob {
+    const int32_t *seq_start;
+    const int32_t *cu_new;
+    int total_new;
+    const uint4 *key;
+    const uint4 *value;
+    int64_t key_stride_v;    // token strides in 16-byte vectors
+    int64_t value_stride_v;
+    uint4 *k_cache;
+    uint4 *v_cache;
+    int64_t *slot_mapping;
+    int row_vecs;            // 16-byte vectors per token row
+    int64_t pool_slots;
+};
+
 // ------------------------------------------------------------------ plan
 __global__ void __launch_bounds__(kPlanThreads)
     decode_plan_kernel(const int32_t *__restrict__ context_lens,
                        const int32_t *__restrict__ cu_seqlens_q,
                        const int32_t *__restrict__ block_tables, int num_seqs, int max_blocks,
                        int num_blocks, int total_q, int32_t *__restrict__ prefix,
-                       StreamEntry *__restrict__ stream, int32_t *status) {
-    extern __shared__ int32_t pref_s[];  // [num_seqs + 1]
+                       StreamEntry *__restrict__ stream, int32_t *status, const KvWriteJob job) {
+    extern __shared__ int32_t pref_s[];  // [num_seqs + 1], then cu_new [num_seqs + 1]
     __shared__ int32_t warp_tot[kPlanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();      // inputs may come from the previous kernel
     grid_dependents_launch();    // the decode kernel may start its prologue
+    if (job.total_new > 0) {
+        // ---- the step's cache write: one warp per new token
+        int32_t *cu_s = pref_s + num_seqs + 1;
+        for (int i = tid; i <= num_seqs; i += kPlanThreads) cu_s[i] = __ldg(job.cu_new + i);
+        __syncthreads();
+        const int warps = kPlanThreads / 32;
+        for (int t = blockIdx.x * warps + warp; t < job.total_new; t += gridDim.x * warps) {
+            int64_t slot = -1;
+            if (lane == 0) {
+                int lo = 0, hi = num_seqs;  // last s with cu_new[s] <= t
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (cu_s[mid] <= t) lo = mid; else hi = mid;
+                }
+                const int64_t pos = (int64_t)__ldg(job.seq_start + lo) + (t - cu_s[lo]);
+                const int64_t logical = pos / kB;
+                if (pos < 0 || logical >= max_blocks) {
+                    set_status(status, PA_ERR_OUT_OF_RANGE);
+                } else {
+                    const int32_t phys = __ldg(block_tables + (int64_t)lo * max_blocks + logical);
+                    if (phys < 0 || phys >= num_blocks) set_status(status, PA_ERR_OUT_OF_RANGE);
+                    else slot = (int64_t)phys * kB + (pos - logical * kB);
+                }
+                job.slot_mapping[t] = slot;
+            }
+            slot = __shfl_sync(0xffffffffu, slot, 0);
+            if (slot < 0 || slot >= job.pool_slots) continue;
+            const uint4 *ks = job.key + t * job.key_stride_v;
+            const uint4 *vs = job.value + t * job.value_stride_v;
+            uint4 *kd = job.k_cache + slot * job.row_vecs;
+            uint4 *vd = job.v_cache + slot * job.row_vecs;
+            for (int i = lane; i < job.row_vecs; i += 32) {
+                const uint4 kv = __ldg(ks + i);
+                const uint4 vv = __ldg(vs + i);
+                kd[i] = kv;
+                vd[i] = vv;
+            }
+        }
+        __syncthreads();
+    }
     int running = 0;
     for (int base = 0; base < num_seqs; base += kPlanThreads) {
         const int s = base + tid;
@@ -618,7 +677,7 @@ size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max
 }
 
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                                cudaStream_t stream, bool timed) {
+                                cudaStream_t stream, bool timed, const KvWriteArgs *write) {
     if (a.num_seqs == 0) return cudaSuccess;
     const WorkspaceLayout w = workspace_layout(a.num_seqs, a.num_heads, a.head_dim, a.max_blocks);
     if (workspace_bytes < w.total) return cudaErrorInvalidValue;
@@ -654,20 +713,38 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
             return cudaErrorNotSupported;
     }
 
-    // plan
-    const size_t plan_smem = sizeof(int32_t) * ((size_t)a.num_seqs + 1);
+    KvWriteJob job = {};
+    if (write) {
+        job.seq_start = write->seq_start;
+        job.cu_new = write->cu_seqlens_new;
+        job.total_new = write->total_new;
+        job.key = static_cast<const uint4 *>(write->key);
+        job.value = static_cast<const uint4 *>(write->value);
+        job.key_stride_v = write->key_stride_tok * 2 / 16;
+        job.value_stride_v = write->value_stride_tok * 2 / 16;
+        job.k_cache = static_cast<uint4 *>(const_cast<void *>(a.k_cache));
+        job.v_cache = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
+        job.slot_mapping = write->slot_mapping;
+        job.row_vecs = a.num_kv_heads * a.head_dim * 2 / 16;
+        job.pool_slots = (int64_t)a.num_blocks * kB;
+    }
+
+    // plan (and the folded cache write)
+    const size_t plan_smem = sizeof(int32_t) * ((size_t)a.num_seqs + 1) * (write ? 2 : 1);
     cudaError_t e = cudaFuncSetAttribute(decode_plan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (e != cudaSuccess) return e;
     const int64_t max_entries = (int64_t)a.num_seqs * a.max_blocks;
     const int sms = device_sm_count();
     int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
+    if (write && plan_grid < (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32))
+        plan_grid = (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32);
     if (plan_grid > 2 * sms) plan_grid = 2 * sms;
     if (plan_grid < 1) plan_grid = 1;
     e = launch_dependent(decode_plan_kernel, dim3(plan_grid), dim3(kPlanThreads), plan_smem, stream,
                          a.context_lens, a.cu_seqlens_q, a.block_tables, a.num_seqs, a.max_blocks,
                          a.num_blocks, a.total_q, reinterpret_cast<int32_t *>(ws + w.prefix),
-                         reinterpret_cast<StreamEntry *>(ws + w.stream), a.status);
+                         reinterpret_cast<StreamEntry *>(ws + w.stream), a.status, job);
     if (e != cudaSuccess) return e;
 
     int grid = sms;

@@ -190,6 +190,57 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     return from_cuda(e);
 }
 
+pa_status pa_decode_step(void *out, const void *q, const void *key, const void *value,
+                         int64_t key_stride_tok, int64_t value_stride_tok, void *k_cache,
+                         void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                         const int32_t *seq_start, const int32_t *cu_seqlens_new, int total_new,
+                         int64_t *slot_mapping, int num_seqs, int num_heads, int num_kv_heads,
+                         int head_dim, int block_size, int max_blocks, int num_blocks, float scale,
+                         pa_dtype dtype, void *workspace, size_t workspace_bytes,
+                         int32_t *dev_status, pa_stream_t stream) {
+    pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                         max_blocks, num_blocks, dtype, scale);
+    if (st != PA_OK) return st;
+    if (total_new < 0) return PA_ERR_INVALID_ARG;
+    const int eb = elem_bytes(dtype);
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (total_new > 0) {
+        if (num_seqs == 0 || !key || !value || !seq_start || !cu_seqlens_new || !slot_mapping)
+            return PA_ERR_INVALID_ARG;
+        if (key_stride_tok < row || value_stride_tok < row) return PA_ERR_INVALID_ARG;
+    }
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned(out, eb) || !aligned(q, eb) || !aligned(k_cache, eb) || !aligned(v_cache, eb))
+        return PA_ERR_INVALID_ARG;
+    AttnArgs a{out, q, k_cache, v_cache, block_tables, context_lens, nullptr,
+               num_seqs, num_seqs, 1, num_heads, num_kv_heads, head_dim, block_size,
+               max_blocks, num_blocks, scale, dtype, dev_status};
+    const bool fused = split_decode_supported(a) && total_new > 0 && aligned(key, 16) &&
+                       aligned(value, 16) && (key_stride_tok * eb) % 16 == 0 &&
+                       (value_stride_tok * eb) % 16 == 0 && (row * eb) % 16 == 0;
+    if (!fused) {
+        if (total_new > 0) {
+            st = pa_compute_slot_mapping(block_tables, num_seqs, max_blocks, seq_start, cu_seqlens_new,
+                                         total_new, block_size, num_blocks, slot_mapping, dev_status, stream);
+            if (st != PA_OK) return st;
+            st = pa_reshape_and_cache(key, value, key_stride_tok, value_stride_tok, k_cache, v_cache,
+                                      slot_mapping, total_new, num_kv_heads, head_dim, block_size,
+                                      num_blocks, dtype, dev_status, stream);
+            if (st != PA_OK) return st;
+        }
+        return pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
+                         num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale, dtype,
+                         workspace, workspace_bytes, dev_status, stream);
+    }
+    const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                 block_size, max_blocks);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
+    KvWriteArgs wr{key, value, key_stride_tok, value_stride_tok, seq_start, cu_seqlens_new,
+                   total_new, slot_mapping};
+    return from_cuda(launch_split_decode(a, workspace, workspace_bytes, (cudaStream_t)stream, true, &wr));
+}
+
 size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
                                         int num_kv_heads, int head_dim, int block_size,
                                         int max_blocks) {

@@ -70,10 +70,24 @@ cudaError_t launch_generic_attention(const AttnArgs &a, int row_filter, cudaStre
 // Persistent TMA + tensor-core split-KV decode (bf16, head_dim 64/128).
 bool split_decode_supported(const AttnArgs &a);
 size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max_blocks);
+// Cache write folded into the decode plan kernel (bf16 rows of 16-byte
+// multiples, 16-byte aligned pointers and strides).
+struct KvWriteArgs {
+    const void *key;
+    const void *value;
+    int64_t key_stride_tok;     // elements
+    int64_t value_stride_tok;
+    const int32_t *seq_start;
+    const int32_t *cu_seqlens_new;
+    int total_new;
+    int64_t *slot_mapping;
+};
+
 // With a.cu_seqlens_q set, only sequences with q_len == 1 are processed and
-// their query/output row is cu_seqlens_q[s].
+// their query/output row is cu_seqlens_q[s].  With `write`, the step's cache
+// write runs in the plan kernel, before any cache read of the decode kernel.
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                                cudaStream_t stream, bool timed);
+                                cudaStream_t stream, bool timed, const KvWriteArgs *write = nullptr);
 
 // tcgen05 causal prefill for sequences with q_len >= 2 (bf16, head_dim 64/128,
 // q-heads per kv-head a power of two up to 16).

@@ -25,7 +25,7 @@ EXPORTS = (
     "pa_status_string", "pa_version", "pa_num_blocks_needed", "pa_compute_slot_mapping",
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
     "pa_varlen_prefill_workspace_size", "pa_varlen_prefill", "pa_get_device_status",
-    "pa_reset_device_status", "pa_set_timing_events", "pa_decode_static_scratch",
+    "pa_reset_device_status", "pa_set_timing_events", "pa_decode_static_scratch", "pa_decode_step",
 )
 STATIC_SCRATCH_BYTES = 24 << 20
 
@@ -76,6 +76,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_reset_device_status.argtypes = [vp, vp]
         L.pa_set_timing_events.restype = i32
         L.pa_set_timing_events.argtypes = [vp, vp]
+        L.pa_decode_step.restype = i32
+        L.pa_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                     i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]
         L.pa_decode_static_scratch.restype = i32
         L.pa_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                                f32, i32, vp, vp]
@@ -204,6 +207,35 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=No
         _opt(dev_status), _stream(stream))
     _check(rc, "pa_decode")
     return out
+
+
+def decode_step(q, key, value, k_cache, v_cache, block_tables, context_lens, seq_start, cu_seqlens_new,
+                scale: float, out=None, slot_mapping=None, workspace=None, dev_status=None, stream=None):
+    """pa_decode_step: slot mapping + cache write of the new tokens + decode, in one call.
+    Returns (slot_mapping, out)."""
+    num_seqs, H, D = q.shape
+    num_blocks, block_size, hkv, d = k_cache.shape
+    max_blocks = block_tables.shape[1]
+    total_new = int(key.shape[0])
+    for name, t in (("key", key), ("value", value)):
+        if t.dim() != 3 or t.shape[1:] != (hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [tokens, {hkv}, {d}] with contiguous rows")
+    if out is None:
+        out = torch.empty_like(q)
+    if slot_mapping is None:
+        slot_mapping = torch.empty(total_new, dtype=torch.int64, device=q.device)
+    need = decode_workspace_size(num_seqs, H, hkv, D, block_size, max_blocks)
+    workspace = _ws(workspace, need, q.device)
+    rc = load().pa_decode_step(
+        _contig(out, "out"), _contig(q, "q"), _dev(key, "key"), _dev(value, "value"), key.stride(0),
+        value.stride(0), _contig(k_cache, "k_cache"), _contig(v_cache, "v_cache"),
+        _contig(block_tables, "block_tables", torch.int32), _contig(context_lens, "context_lens", torch.int32),
+        _contig(seq_start, "seq_start", torch.int32), _contig(cu_seqlens_new, "cu_seqlens_new", torch.int32),
+        total_new, _contig(slot_mapping, "slot_mapping", torch.int64), num_seqs, H, hkv, D, block_size,
+        max_blocks, num_blocks, float(scale), _dtype_code(q), _contig(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _opt(dev_status), _stream(stream))
+    _check(rc, "pa_decode_step")
+    return slot_mapping, out
 
 
 def varlen_prefill(q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -312,6 +312,60 @@ def test_stale_workspace_contents_do_not_matter(name):
     assert torch.equal(clean, dirty)
 
 
+@pytest.mark.parametrize("name", ["gqa_small", "tiny", "long_small", "mha_small", "mqa_small", "d64_bf16"])
+def test_fused_decode_step_equals_separate_calls(name):
+    """pa_decode_step = slot mapping + cache write + decode, bit for bit."""
+    a = SMALL[name](12)
+    b = SMALL[name](12)
+    slots_a, out_a = gpu_step(a)                   # three separate calls
+    slots_b, out_b = pa.decode_step(b.q, b.key, b.value, b.k_cache, b.v_cache, b.block_tables,
+                                    b.context_lens, b.seq_start, b.cu_seqlens_q, b.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(slots_a, slots_b)
+    bits = torch.int16 if a.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(a.k_cache.view(bits), b.k_cache.view(bits))
+    assert torch.equal(a.v_cache.view(bits), b.v_cache.view(bits))
+    assert torch.equal(out_a, out_b)
+
+
+def test_fused_decode_step_full_size_matches_oracle():
+    w = W.make("gqa256_bf16", 2, oracle_blocks, device=DEV)
+    wc = w.to("cpu")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots, out = pa.decode_step(w.q, w.key, w.value, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                w.seq_start, w.cu_seqlens_q, w.scale, dev_status=status)
+    torch.cuda.synchronize()
+    assert pa.get_device_status(status) == 0
+    ref_slots = oracle_write(wc)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    assert torch.equal(w.k_cache.cpu().view(torch.int16), wc.k_cache.view(torch.int16))
+    compare(to_f64(out), oracle_attention(wc), torch.bfloat16, "decode step gqa256")
+
+
+def test_fused_decode_step_token_strided_and_bad_slot():
+    w = SMALL["gqa_small"](14)
+    T, hkv, d = w.key.shape
+    fused = torch.empty(T, 3, hkv, d, dtype=w.dtype, device=DEV)
+    fused[:, 1] = w.key
+    fused[:, 2] = w.value
+    ref = SMALL["gqa_small"](14)
+    _, out_ref = gpu_step(ref)
+    _, out = pa.decode_step(w.q, fused[:, 1], fused[:, 2], w.k_cache, w.v_cache, w.block_tables,
+                            w.context_lens, w.seq_start, w.cu_seqlens_q, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_ref)
+    # an out-of-range table entry on a new token's block: status set, no fault
+    bt = w.block_tables.clone()
+    s = 3
+    lb = int(w.seq_start[s]) // 16
+    bt[s, lb] = w.num_blocks + 7
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots, _ = pa.decode_step(w.q, w.key, w.value, w.k_cache, w.v_cache, bt, w.context_lens, w.seq_start,
+                              w.cu_seqlens_q, w.scale, dev_status=status)
+    assert pa.get_device_status(status) == pa.ERR_OUT_OF_RANGE
+    assert int(slots[s]) == -1
+
+
 def test_workspace_too_small_is_rejected():
     w = SMALL["gqa_small"](1)
     ws = torch.empty(64, dtype=torch.uint8, device=DEV)
