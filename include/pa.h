@@ -217,6 +217,30 @@ PA_API pa_status pa_decode_step(void *out, const void *q, const void *key, const
                                 int num_blocks, float scale, pa_dtype dtype, void *workspace,
                                 size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream);
 
+/*
+ * Whole-block copies between KV pools ([kwkr] §1.3 swap space; §2.2: the
+ * block manager moves inactive physical blocks to host memory and back;
+ * §1.3: physical blocks shared by several requests).  For each pair i,
+ * (src, dst) = (pairs[2i], pairs[2i+1]): block src of the source pools is
+ * copied byte for byte to block dst of the destination pools, K and V.
+ * One call covers:
+ *  - fork / copy inside one pool (source and destination pools the same);
+ *  - swap out / in between the device pool and a host pool, whose memory
+ *    must be reachable from the device (cudaHostAlloc / cudaHostRegister);
+ *  - pack / unpack a request's blocks to / from a contiguous buffer (a pool
+ *    whose blocks are numbered 0 .. n-1).
+ *  block_bytes  bytes of one block of one pool: block_size*num_kv_heads*head_dim*elem
+ *  pairs        device int32 [num_pairs][2]; a negative entry skips the pair;
+ *               an entry past its pool's block count sets PA_ERR_OUT_OF_RANGE
+ *               in *dev_status and the pair is skipped
+ * Precondition (not checked on the device): destinations are distinct and no
+ * destination block is also a source in the same call.
+ */
+PA_API pa_status pa_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                                int64_t block_bytes, int src_num_blocks, int dst_num_blocks,
+                                const int32_t *pairs, int num_pairs, int32_t *dev_status,
+                                pa_stream_t stream);
+
 /* Workspace bytes pa_varlen_prefill needs for these sizes. */
 PA_API size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
                                         int num_kv_heads, int head_dim, int block_size,

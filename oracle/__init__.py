@@ -76,6 +76,7 @@ def lib():
             L.or_attention_partial.argtypes = [ctypes.POINTER(_Problem), i32, i32, i32,
                                                ctypes.c_longlong, ctypes.c_longlong, dp, dp, dp]
             L.or_merge_partials.argtypes = [dp, dp, dp, i32, i32, dp]
+            L.or_copy_blocks.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp, i32]
             L.or_max_threads.restype = i32
             _lib = L
     return _lib
@@ -232,3 +233,29 @@ def merge_partials(m, l, o) -> np.ndarray:
                                  int(m.size), int(o.shape[-1]), out.ctypes.data)
     _check(rc, "merge_partials")
     return out
+
+
+# ---------------------------------------------------------------- block copy (swap, fork, pack)
+def validate_block_pairs(pairs) -> None:
+    """Precondition of one copy call: destinations distinct, and no block is
+    both written and read in the same call."""
+    p = np.asarray(pairs).reshape(-1, 2)
+    live = p[(p[:, 0] >= 0) & (p[:, 1] >= 0)]
+    if np.unique(live[:, 1]).size != live.shape[0]:
+        raise OracleError("duplicate destination blocks in one copy")
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, pairs) -> None:
+    """Copies whole blocks src -> dst (pairs [n, 2] int32), in place on CPU pools."""
+    for t in (src_k, src_v, dst_k, dst_v):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("pools must be contiguous CPU tensors")
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    validate_block_pairs(pairs)
+    block_bytes = src_k[0].numel() * src_k.element_size()
+    if dst_k[0].numel() * dst_k.element_size() != block_bytes:
+        raise ValueError("source and destination blocks differ in size")
+    rc = lib().or_copy_blocks(_ptr(src_k), _ptr(src_v), _ptr(dst_k), _ptr(dst_v), block_bytes,
+                              int(src_k.shape[0]), int(dst_k.shape[0]), pairs.ctypes.data,
+                              int(pairs.shape[0]))
+    _check(rc, "copy_blocks")

@@ -377,6 +377,28 @@ int or_merge_partials(const double *m, const double *l, const double *o,
     return OR_OK;
 }
 
+/* ---- block copy: swap in/out, fork, pack/unpack ([kwkr] §1.3 swap space,
+ * §2.2 the block manager moves inactive physical blocks to host memory and
+ * back; §1.3 blocks shared by several requests).  For each pair (src, dst),
+ * the whole block src of the source pools is copied byte for byte to block
+ * dst of the destination pools.  A negative src or dst skips the pair. */
+int or_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                   int64_t block_bytes, int src_num_blocks, int dst_num_blocks,
+                   const int32_t *pairs, int num_pairs)
+{
+    if (block_bytes <= 0 || num_pairs < 0) return OR_ERR_ARG;
+    for (int i = 0; i < num_pairs; ++i) {
+        int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || dst < 0) continue;
+        if (src >= src_num_blocks || dst >= dst_num_blocks) return OR_ERR_RANGE;
+        memcpy((char *)dst_k + (int64_t)dst * block_bytes,
+               (const char *)src_k + (int64_t)src * block_bytes, (size_t)block_bytes);
+        memcpy((char *)dst_v + (int64_t)dst * block_bytes,
+               (const char *)src_v + (int64_t)src * block_bytes, (size_t)block_bytes);
+    }
+    return OR_OK;
+}
+
 int or_max_threads(void)
 {
 #ifdef _OPENMP

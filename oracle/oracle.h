@@ -66,6 +66,10 @@ int or_attention_partial(const or_problem *pr, int s, int i, int h,
 int or_merge_partials(const double *m, const double *l, const double *o,
                       int nparts, int head_dim, double *out);
 
+int or_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                   int64_t block_bytes, int src_num_blocks, int dst_num_blocks,
+                   const int32_t *pairs, int num_pairs);
+
 int or_max_threads(void);
 
 #ifdef __cplusplus

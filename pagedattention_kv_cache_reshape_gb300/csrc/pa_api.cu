@@ -241,6 +241,22 @@ pa_status pa_decode_step(void *out, const void *q, const void *key, const void *
     return from_cuda(launch_split_decode(a, workspace, workspace_bytes, (cudaStream_t)stream, true, &wr));
 }
 
+pa_status pa_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                         int64_t block_bytes, int src_num_blocks, int dst_num_blocks,
+                         const int32_t *pairs, int num_pairs, int32_t *dev_status,
+                         pa_stream_t stream) {
+    if (num_pairs < 0 || block_bytes <= 0 || src_num_blocks < 0 || dst_num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if (block_bytes % 2 != 0) return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !pairs) return PA_ERR_INVALID_ARG;
+    if (!aligned(src_k, 2) || !aligned(src_v, 2) || !aligned(dst_k, 2) || !aligned(dst_v, 2))
+        return PA_ERR_INVALID_ARG;
+    return from_cuda(launch_copy_blocks(src_k, src_v, dst_k, dst_v, block_bytes, src_num_blocks,
+                                        dst_num_blocks, pairs, num_pairs, dev_status,
+                                        (cudaStream_t)stream));
+}
+
 size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads,
                                         int num_kv_heads, int head_dim, int block_size,
                                         int max_blocks) {

@@ -62,6 +62,12 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, int64_t
                                      int num_blocks, int elem_bytes, int32_t *status,
                                      cudaStream_t stream);
 
+// Whole-block copies between pools (device or device-accessible host memory).
+cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                               int64_t block_bytes, int src_num_blocks, int dst_num_blocks,
+                               const int32_t *pairs, int num_pairs, int32_t *status,
+                               cudaStream_t stream);
+
 // CUDA-core attention for every supported shape and dtype (one CTA per query
 // row and kv-head).  row_filter selects the sequences it computes.
 constexpr int kAllRows = 0, kSkipSingleRows = 1, kOnlySingleRows = 2;

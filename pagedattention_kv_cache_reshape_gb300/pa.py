@@ -26,6 +26,7 @@ EXPORTS = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
     "pa_varlen_prefill_workspace_size", "pa_varlen_prefill", "pa_get_device_status",
     "pa_reset_device_status", "pa_set_timing_events", "pa_decode_static_scratch", "pa_decode_step",
+    "pa_copy_blocks",
 )
 STATIC_SCRATCH_BYTES = 24 << 20
 
@@ -76,6 +77,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_reset_device_status.argtypes = [vp, vp]
         L.pa_set_timing_events.restype = i32
         L.pa_set_timing_events.argtypes = [vp, vp]
+        L.pa_copy_blocks.restype = i32
+        L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp, i32, vp, vp]
         L.pa_decode_step.restype = i32
         L.pa_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                      i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]
@@ -236,6 +239,26 @@ def decode_step(q, key, value, k_cache, v_cache, block_tables, context_lens, seq
         workspace.numel() * workspace.element_size(), _opt(dev_status), _stream(stream))
     _check(rc, "pa_decode_step")
     return slot_mapping, out
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, pairs, dev_status=None, stream=None):
+    """pa_copy_blocks: whole blocks src -> dst between pools of equal block shape.
+    Pools may be device tensors or pinned host tensors (reachable from the device);
+    pairs is a device int32 tensor [n, 2]."""
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype:
+        raise ValueError("source and destination pools must share block shape and dtype")
+    for name, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    pairs = pairs.reshape(-1, 2)
+    block_bytes = src_k[0].numel() * src_k.element_size()
+    rc = load().pa_copy_blocks(src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(),
+                               block_bytes, int(src_k.shape[0]), int(dst_k.shape[0]),
+                               _contig(pairs, "pairs", torch.int32), int(pairs.shape[0]), _opt(dev_status),
+                               _stream(stream))
+    _check(rc, "pa_copy_blocks")
 
 
 def varlen_prefill(q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens, scale: float,

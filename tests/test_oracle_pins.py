@@ -429,3 +429,46 @@ def test_merge_of_outlier_partials_is_stable():
     o = np.array([[3.0, 6.0], [2.0, -2.0], [5.0, 5.0]])
     out = oracle.merge_partials(m, l, o)
     np.testing.assert_allclose(out, [1.0, -1.0], rtol=0, atol=1e-15)
+
+
+# ------------------------------------------------------------------ block copy (swap / fork / pack)
+
+def test_copy_blocks_moves_whole_blocks_and_nothing_else():
+    B, hkv, d = 16, 2, 8
+    src_k = torch.randn(6, B, hkv, d).to(torch.bfloat16)
+    src_v = torch.randn(6, B, hkv, d).to(torch.bfloat16)
+    dst_k = torch.zeros(4, B, hkv, d, dtype=torch.bfloat16)
+    dst_v = torch.zeros_like(dst_k)
+    oracle.copy_blocks(src_k, src_v, dst_k, dst_v, [[5, 0], [2, 3], [-1, 1], [0, -1]])
+    assert torch.equal(dst_k[0], src_k[5]) and torch.equal(dst_v[0], src_v[5])
+    assert torch.equal(dst_k[3], src_k[2]) and torch.equal(dst_v[3], src_v[2])
+    assert (dst_k[1:3] == 0).all() and (dst_v[1:3] == 0).all()
+
+
+def test_copy_blocks_pack_then_unpack_restores_a_request():
+    # pack a request's scattered blocks into a contiguous buffer, wipe them,
+    # unpack into other physical blocks: attention through the new table is unchanged
+    P = _dense_problem(111, [70], [1], 4, 2, 32, extra_blocks=8)
+    base = _oracle_out(P)
+    bt = P["bt"][0]
+    nb = oracle.num_blocks_needed(70, 16)
+    k_buf = torch.empty(nb, *P["kpool"].shape[1:], dtype=P["kpool"].dtype)
+    v_buf = torch.empty_like(k_buf)
+    pack = [[int(bt[i]), i] for i in range(nb)]
+    oracle.copy_blocks(P["kpool"], P["vpool"], k_buf, v_buf, pack)
+    free = sorted(set(range(P["kpool"].shape[0])) - set(bt[:nb].tolist()))
+    new_ids = free[:nb]
+    P["kpool"][bt[:nb].long()] = float("nan")
+    P["vpool"][bt[:nb].long()] = float("nan")
+    oracle.copy_blocks(k_buf, v_buf, P["kpool"], P["vpool"], [[i, new_ids[i]] for i in range(nb)])
+    P["bt"] = P["bt"].clone()
+    P["bt"][0, :nb] = torch.tensor(new_ids, dtype=torch.int32)
+    assert np.array_equal(_oracle_out(P), base)
+
+
+def test_copy_blocks_rejects_bad_pairs():
+    k = torch.zeros(3, 16, 1, 8)
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(k, k.clone(), k.clone(), k.clone(), [[0, 1], [2, 1]])   # same destination
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(k, k.clone(), k.clone(), k.clone(), [[3, 0]])           # outside the source
