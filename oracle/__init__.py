@@ -58,6 +58,7 @@ class _Problem(ctypes.Structure):
         ("num_seqs", ctypes.c_int), ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
         ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int), ("max_blocks", ctypes.c_int),
         ("num_blocks", ctypes.c_int), ("dtype", ctypes.c_int), ("scale", ctypes.c_double),
+        ("non_causal", ctypes.c_int),
     ]
 
 
@@ -167,7 +168,7 @@ class Problem:
     """Keeps the CPU tensors alive while the C struct points into them."""
 
     def __init__(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                 cu_seqlens_q=None):
+                 cu_seqlens_q=None, causal: bool = True):
         self.q = _cpu(q)
         self.k_cache = _cpu(k_cache)
         self.v_cache = _cpu(v_cache)
@@ -186,13 +187,13 @@ class Problem:
             cu_seqlens_q=None if self.cu is None else _ptr(self.cu),
             num_seqs=int(self.bt.shape[0]), num_heads=self.num_heads, num_kv_heads=hkv,
             head_dim=d, block_size=B, max_blocks=int(self.bt.shape[1]), num_blocks=num_blocks,
-            dtype=_dtype_code(self.q), scale=float(scale))
+            dtype=_dtype_code(self.q), scale=float(scale), non_causal=0 if causal else 1)
 
 
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                    cu_seqlens_q=None, nthreads: int = 1) -> np.ndarray:
+                    cu_seqlens_q=None, nthreads: int = 1, causal: bool = True) -> np.ndarray:
     """Full output [rows, num_heads, head_dim] in float64."""
-    pr = Problem(q, k_cache, v_cache, block_tables, context_lens, scale, cu_seqlens_q)
+    pr = Problem(q, k_cache, v_cache, block_tables, context_lens, scale, cu_seqlens_q, causal)
     out = np.zeros((pr.rows, pr.num_heads, pr.head_dim), dtype=np.float64)
     rc = lib().or_paged_attention(ctypes.byref(pr.c), out.ctypes.data, int(nthreads))
     _check(rc, "paged_attention")
@@ -200,9 +201,10 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: floa
 
 
 def paged_attention_rows(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                         rows, heads, cu_seqlens_q=None, nthreads: int = 1) -> np.ndarray:
+                         rows, heads, cu_seqlens_q=None, nthreads: int = 1,
+                         causal: bool = True) -> np.ndarray:
     """Output of selected (row, head) pairs: [nsel, head_dim] float64."""
-    pr = Problem(q, k_cache, v_cache, block_tables, context_lens, scale, cu_seqlens_q)
+    pr = Problem(q, k_cache, v_cache, block_tables, context_lens, scale, cu_seqlens_q, causal)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     heads = np.ascontiguousarray(np.asarray(heads, dtype=np.int32))
     out = np.zeros((rows.size, pr.head_dim), dtype=np.float64)

@@ -38,7 +38,11 @@
  *  - context_lens counts every token the query may see, including the ones
  *    being written in this step; query i of a sequence with q_len new tokens
  *    sits at position ctx - q_len + i and sees keys 0..that position;
- *  - q-head h uses kv-head h / (num_heads / num_kv_heads).
+ *  - q-head h uses kv-head h / (num_heads / num_kv_heads);
+ *  - encode-only attention (the embedding workload of "vLLMつかったら、
+ *    ベクトル検索サーバーが高速化して安定性も向上した": vector search only
+ *    encodes) drops the causal mask: every query row of a sequence sees all
+ *    of that sequence's context_lens[s] keys, and still no other sequence's.
  *
  * Parity pins: every function is pinned by tests (worked examples printed
  * on the pages, closed forms, invariants, fp64 torch SDPA, brute force); see
@@ -203,6 +207,7 @@ static int attend_one(const or_problem *pr, int s, int i, int h, double *o)
     if (i < 0 || i >= q_len) return OR_ERR_ARG;
     int64_t pos = (int64_t)ctx - q_len + i;   /* position of this query */
     int64_t n = pos + 1;                      /* keys 0..pos are visible */
+    if (pr->non_causal) n = ctx;              /* encode: the whole sequence */
     double *x = (double *)malloc((size_t)n * sizeof(double));
     if (!x) return OR_ERR_ARG;
     rc = logits(pr, s, first + i, h, 0, n, x);

@@ -37,6 +37,7 @@ typedef struct {
     int num_blocks;
     int dtype;        /* OR_F32 or OR_BF16: q and both pools */
     double scale;
+    int non_causal;   /* 1: every query row sees all context_lens[s] keys (encode) */
 } or_problem;
 
 long long or_num_blocks_needed(long long num_tokens, long long block_size);

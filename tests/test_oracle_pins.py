@@ -221,7 +221,7 @@ def _dense_problem(seed, ctx_list, q_lens, H, Hkv, D, B=16, dtype=torch.float64,
                 scale=W.fp32_scale(D), H=H, Hkv=Hkv, D=D, B=B)
 
 
-def _sdpa_reference(P):
+def _sdpa_reference(P, causal=True):
     """torch fp64 SDPA per sequence on the dense K/V, bottom-right causal, GQA by repeat."""
     H, Hkv = P["H"], P["Hkv"]
     outs = []
@@ -235,7 +235,10 @@ def _sdpa_reference(P):
         i = torch.arange(ql).view(-1, 1)
         j = torch.arange(c).view(1, -1)
         mask = j <= (c - ql + i)
-        o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=P["scale"])
+        if causal:
+            o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=P["scale"])
+        else:
+            o = F.scaled_dot_product_attention(q, k, v, scale=P["scale"])
         outs.append(o[0].permute(1, 0, 2))
     return torch.cat(outs).numpy()
 
@@ -269,6 +272,26 @@ def test_causal_prefill_matches_fp64_sdpa():
     qlen = [40, 5, 1, 37, 1]
     P = _dense_problem(5, ctx, qlen, 8, 2, 64)
     np.testing.assert_allclose(_oracle_out(P), _sdpa_reference(P), rtol=0, atol=1e-12)
+
+
+def test_encode_only_matches_unmasked_fp64_sdpa():
+    # whole prompts (the embedding workload) and chunks over a cached prefix
+    ctx = [40, 17, 1, 90, 33]
+    qlen = [40, 17, 1, 37, 2]
+    P = _dense_problem(6, ctx, qlen, 8, 2, 64)
+    out = oracle.paged_attention(P["q"], P["kpool"], P["vpool"], P["bt"], P["ctx"], P["scale"],
+                                 cu_seqlens_q=P["cu"], causal=False)
+    np.testing.assert_allclose(out, _sdpa_reference(P, causal=False), rtol=0, atol=1e-12)
+    # every row of a sequence sees the same keys: equal queries give equal rows
+    P["q"][1] = P["q"][0]
+    out = oracle.paged_attention(P["q"], P["kpool"], P["vpool"], P["bt"], P["ctx"], P["scale"],
+                                 cu_seqlens_q=P["cu"], causal=False)
+    assert np.array_equal(out[0], out[1])
+    # the last row of each sequence is the same in both modes
+    causal = _oracle_out(P)
+    for s in range(len(ctx)):
+        r = int(P["cu"][s + 1]) - 1
+        assert np.array_equal(out[r], causal[r])
 
 
 def test_closed_form_single_key_returns_value():
