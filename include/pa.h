@@ -272,6 +272,22 @@ PA_API pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_s
                             size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream);
 
 /*
+ * Encode-only varlen paged attention: pa_varlen_prefill without the causal
+ * mask.  Every query row of sequence s attends to all context_lens[s] keys of
+ * s, and still to no other sequence's ("vLLMつかったら、ベクトル検索サーバーが
+ * 高速化して安定性も向上した": an embedding / vector-search server only
+ * encodes).  Same arguments, layouts, workspace (pa_varlen_prefill_workspace_size)
+ * and error behaviour as pa_varlen_prefill.
+ */
+PA_API pa_status pa_varlen_encode(void *out, const void *q, const int32_t *cu_seqlens_q,
+                                  const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int total_q, int max_q_len, int num_heads,
+                                  int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                                  int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream);
+
+/*
  * Copies the device status word to *host_out after synchronising `stream`.
  * Returns PA_ERR_CUDA if the copy fails (for example after a sticky fault).
  */

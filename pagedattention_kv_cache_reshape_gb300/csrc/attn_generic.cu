@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(kThreads)
         if (tid == 0) set_status(a.status, PA_ERR_OUT_OF_RANGE);
         return;
     }
-    const int n_keys = ctx - q_len + i + 1;  // keys 0 .. position of this query
+    // keys 0 .. position of this query (causal), or the whole sequence (encode)
+    const int n_keys = a.causal ? ctx - q_len + i + 1 : ctx;
 
     const T *q = static_cast<const T *>(a.q) + ((int64_t)row * a.num_heads + g * G) * D;
     for (int idx = tid; idx < G * D; idx += kThreads) {

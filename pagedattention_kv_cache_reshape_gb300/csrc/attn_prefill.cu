@@ -66,6 +66,7 @@ struct PrefillParams {
     int num_blocks;
     float scale_log2;
     int32_t *status;
+    int causal;      // 0: encode-only, every row sees the whole sequence
 };
 
 // ------------------------------------------------------------------ plan
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nrows_all = min(kMT * POS, q_len - i0);  // valid positions of the CTA
     if (nrows_all <= 0) return;
     const int pos_base = ctx - q_len + i0;
-    const int pos_last = pos_base + nrows_all - 1;
+    const int pos_last = p.causal ? pos_base + nrows_all - 1 : ctx - 1;
     const int nkv = pos_last / BN + 1;
     const int nb = (ctx + kB - 1) / kB;
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
@@ -325,7 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h_local = r >> p.pos_shift;
         const int i = t * POS + (r & (POS - 1));          // position index within the CTA
         const bool row_valid = i < nrows_all;
-        const int pos = pos_base + (row_valid ? i : nrows_all - 1);
+        // last visible key of this row: its position (causal) or the sequence end
+        const int pos = p.causal ? pos_base + (row_valid ? i : nrows_all - 1) : ctx - 1;
+        const int first_pos = p.causal ? pos_base + t * POS : ctx - 1;   // smallest pos of the tile
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int t_tail = ctx & (kB - 1);          // valid tokens in the last block (0 = full)
         const int lb_last = (ctx - 1) / kB;
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sv[BN];
             float mx = -INFINITY;
             const int key0 = j * BN;
-            const bool diag = key0 + BN - 1 > pos_base + t * POS;   // a key past some row of this tile
+            const bool diag = key0 + BN - 1 > first_pos;   // a key past some row of this tile
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
@@ -565,6 +568,7 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     prm.num_blocks = a.num_blocks;
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.status = a.status;
+    prm.causal = a.causal;
     return a.head_dim == 64 ? launch_main<64>(mq, mk, mv, prm, capacity, a.num_kv_heads, stream)
                             : launch_main<128>(mq, mk, mv, prm, capacity, a.num_kv_heads, stream);
 }

@@ -267,13 +267,16 @@ size_t pa_varlen_prefill_workspace_size(int num_seqs, int total_q, int num_heads
            prefill_workspace(num_seqs, total_q);
 }
 
-pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_q,
-                            const void *k_cache, const void *v_cache,
-                            const int32_t *block_tables, const int32_t *context_lens,
-                            int num_seqs, int total_q, int max_q_len, int num_heads,
-                            int num_kv_heads, int head_dim, int block_size, int max_blocks,
-                            int num_blocks, float scale, pa_dtype dtype, void *workspace,
-                            size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+pa_status varlen_attention(void *out, const void *q, const int32_t *cu_seqlens_q,
+                           const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int num_seqs, int total_q, int max_q_len,
+                           int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_blocks, int num_blocks, float scale, pa_dtype dtype,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           pa_stream_t stream, int causal) {
     pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                          max_blocks, num_blocks, dtype, scale);
     if (st != PA_OK) return st;
@@ -286,7 +289,7 @@ pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_
         return PA_ERR_INVALID_ARG;
     AttnArgs a{out, q, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q,
                num_seqs, total_q, max_q_len, num_heads, num_kv_heads, head_dim, block_size,
-               max_blocks, num_blocks, scale, dtype, dev_status};
+               max_blocks, num_blocks, scale, dtype, dev_status, causal};
     cudaStream_t s = (cudaStream_t)stream;
     const bool fast_decode = split_decode_supported(a);
     const bool fast_prefill = prefill_tc_supported(a);
@@ -316,6 +319,35 @@ pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_
     }
     timing_end(s);
     return from_cuda(e);
+}
+}  // namespace
+
+extern "C" {
+
+pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_seqlens_q,
+                            const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens,
+                            int num_seqs, int total_q, int max_q_len, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                            int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream) {
+    return varlen_attention(out, q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens,
+                            num_seqs, total_q, max_q_len, num_heads, num_kv_heads, head_dim,
+                            block_size, max_blocks, num_blocks, scale, dtype, workspace,
+                            workspace_bytes, dev_status, stream, 1);
+}
+
+pa_status pa_varlen_encode(void *out, const void *q, const int32_t *cu_seqlens_q,
+                           const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int num_seqs, int total_q, int max_q_len,
+                           int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_blocks, int num_blocks, float scale, pa_dtype dtype,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           pa_stream_t stream) {
+    return varlen_attention(out, q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens,
+                            num_seqs, total_q, max_q_len, num_heads, num_kv_heads, head_dim,
+                            block_size, max_blocks, num_blocks, scale, dtype, workspace,
+                            workspace_bytes, dev_status, stream, 0);
 }
 
 pa_status pa_get_device_status(const int32_t *dev_status, int32_t *host_out, pa_stream_t stream) {

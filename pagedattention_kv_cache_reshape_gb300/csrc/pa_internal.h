@@ -34,6 +34,7 @@ struct AttnArgs {
     float scale;
     pa_dtype dtype;
     int32_t *status;
+    int causal = 1;  // 0: every query row sees all context_lens[s] keys (encode-only)
 };
 
 constexpr int kBlockSize = 16;     // tokens per cache block (the only one built)

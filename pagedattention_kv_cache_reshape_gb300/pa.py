@@ -26,7 +26,7 @@ EXPORTS = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
     "pa_varlen_prefill_workspace_size", "pa_varlen_prefill", "pa_get_device_status",
     "pa_reset_device_status", "pa_set_timing_events", "pa_decode_static_scratch", "pa_decode_step",
-    "pa_copy_blocks",
+    "pa_copy_blocks", "pa_varlen_encode",
 )
 STATIC_SCRATCH_BYTES = 24 << 20
 
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_varlen_prefill.restype = i32
         L.pa_varlen_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                         i32, i32, f32, i32, vp, sz, vp, vp]
+        L.pa_varlen_encode.restype = i32
+        L.pa_varlen_encode.argtypes = L.pa_varlen_prefill.argtypes
         L.pa_get_device_status.restype = i32
         L.pa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
         L.pa_reset_device_status.restype = i32
@@ -262,8 +264,10 @@ def copy_blocks(src_k, src_v, dst_k, dst_v, pairs, dev_status=None, stream=None)
 
 
 def varlen_prefill(q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                   max_q_len: int, out=None, workspace=None, dev_status=None, stream=None):
-    """pa_varlen_prefill over a concatenated super-sequence: q [total_q, H, D]."""
+                   max_q_len: int, out=None, workspace=None, dev_status=None, stream=None,
+                   causal: bool = True):
+    """pa_varlen_prefill (causal) or pa_varlen_encode (causal=False) over a
+    concatenated super-sequence: q [total_q, H, D]."""
     total_q, H, D = q.shape
     num_blocks, block_size, hkv, d = k_cache.shape
     num_seqs, max_blocks = block_tables.shape
@@ -271,14 +275,15 @@ def varlen_prefill(q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens
         out = torch.empty_like(q)
     need = varlen_prefill_workspace_size(num_seqs, total_q, H, hkv, D, block_size, max_blocks)
     workspace = _ws(workspace, need, q.device)
-    rc = load().pa_varlen_prefill(
+    fn = load().pa_varlen_prefill if causal else load().pa_varlen_encode
+    rc = fn(
         _contig(out, "out"), _contig(q, "q"), _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32),
         _contig(k_cache, "k_cache"), _contig(v_cache, "v_cache"),
         _contig(block_tables, "block_tables", torch.int32), _contig(context_lens, "context_lens", torch.int32),
         num_seqs, total_q, int(max_q_len), H, hkv, D, block_size, max_blocks, num_blocks, float(scale),
         _dtype_code(q), _contig(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _opt(dev_status), _stream(stream))
-    _check(rc, "pa_varlen_prefill")
+    _check(rc, "pa_varlen_prefill" if causal else "pa_varlen_encode")
     return out
 
 

@@ -44,12 +44,12 @@ def oracle_write(w_cpu: W.Workload):
     return slots
 
 
-def oracle_attention(w_cpu: W.Workload, nthreads=None):
+def oracle_attention(w_cpu: W.Workload, nthreads=None, causal=True):
     nthreads = nthreads or max(1, oracle.max_threads())
     return oracle.paged_attention(w_cpu.q, w_cpu.k_cache, w_cpu.v_cache, w_cpu.block_tables,
                                   w_cpu.context_lens, w_cpu.scale,
                                   cu_seqlens_q=None if w_cpu.decode_only else w_cpu.cu_seqlens_q,
-                                  nthreads=nthreads)
+                                  nthreads=nthreads, causal=causal)
 
 
 def oracle_rows(w_cpu: W.Workload, rows, heads, nthreads=None):

@@ -96,6 +96,29 @@ def test_prefill_shapes_every_output(name):
     _run_and_check_all(w)
 
 
+@pytest.mark.parametrize("name", list(PREFILL_CASES) + ["fp32_encode"])
+def test_encode_only_every_output(name):
+    """pa_varlen_encode: no causal mask, each row sees its whole sequence."""
+    if name == "fp32_encode":
+        H, Hkv, D, ql, ctx, dt = 8, 2, 64, [20, 1, 7], [20, 33, 40], torch.float32
+    else:
+        (H, Hkv, D, ql, ctx), dt = PREFILL_CASES[name], torch.bfloat16
+    w = W.build(name, seed=23, blocks_needed=oracle_blocks, dtype=dt, num_heads=H, num_kv_heads=Hkv,
+                head_dim=D, block_size=16, q_lens=ql, context_lens=ctx, device=DEV)
+    wc = w.to("cpu")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots = pa.compute_slot_mapping(w.block_tables, w.seq_start, w.cu_seqlens_q, w.num_blocks, w.total_q)
+    pa.reshape_and_cache(w.key, w.value, w.k_cache, w.v_cache, slots)
+    out = pa.varlen_prefill(w.q, w.cu_seqlens_q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                            w.scale, int(w.q_lens.max()), dev_status=status, causal=False)
+    torch.cuda.synchronize()
+    assert pa.get_device_status(status) == 0
+    oracle_write(wc)
+    ref = oracle.paged_attention(wc.q, wc.k_cache, wc.v_cache, wc.block_tables, wc.context_lens, wc.scale,
+                                 cu_seqlens_q=wc.cu_seqlens_q, nthreads=8, causal=False)
+    compare(to_f64(out), ref, dt, name + " encode")
+
+
 def test_tiny_config_full():
     # configuration: 4 sequences, context {1,16,17,50}, fp32, 32-block pool
     for seed in (0, 3, 4):
