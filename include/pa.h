@@ -288,6 +288,51 @@ PA_API pa_status pa_varlen_encode(void *out, const void *q, const int32_t *cu_se
                                   size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream);
 
 /*
+ * Host block manager (no GPU work): the physical block pool that produces the
+ * block tables above.  [iitog] allocate_slots paragraph: a pool of free blocks;
+ * a request that grows by n tokens gets ceil((cached + n) / block_size) minus
+ * its current number of blocks, when the pool holds that many, and nothing
+ * otherwise (the scheduler then preempts or skips it).  [kwkr] §2.2: a
+ * finished request's blocks return to the pool at once; §1.3: blocks can be
+ * referenced read-only by several tables, so a block returns to the pool
+ * when its last reference is freed.  All calls lock an internal mutex.
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* Pool of num_blocks blocks of block_size tokens; NULL on bad arguments. */
+PA_API pa_block_manager *pa_block_manager_create(int num_blocks, int block_size,
+                                                 int max_blocks_per_seq);
+PA_API void pa_block_manager_destroy(pa_block_manager *m);
+/* Free blocks in the pool, or -1 for a NULL manager. */
+PA_API int pa_block_manager_num_free(pa_block_manager *m);
+/* References to `block` (0 = free), or -1 when out of range. */
+PA_API int pa_block_manager_refcount(pa_block_manager *m, int block);
+/*
+ * allocate_slots: room for num_new_tokens more tokens of seq_id (created on
+ * first use).  PA_OK; PA_ERR_OUT_OF_RANGE when the pool lacks the blocks
+ * (nothing is taken); PA_ERR_INVALID_ARG past max_blocks_per_seq;
+ * PA_ERR_UNSUPPORTED when the last block is partly filled and shared (a write
+ * into a shared block would need copy-on-write, which is not provided).
+ */
+PA_API pa_status pa_allocate_slots(pa_block_manager *m, int64_t seq_id, int num_new_tokens);
+/* Drops seq_id's references; blocks no table references go back to the pool. */
+PA_API pa_status pa_free_sequence(pa_block_manager *m, int64_t seq_id);
+/*
+ * child_id (new) references the first num_tokens tokens of parent_id, which
+ * must be whole blocks (PA_ERR_UNSUPPORTED otherwise): a shared read-only
+ * prefix such as a common system prompt, or a fork for parallel sampling.
+ */
+PA_API pa_status pa_share_prefix(pa_block_manager *m, int64_t parent_id, int64_t child_id,
+                                 int num_tokens);
+/*
+ * Host int32 block_tables [n][max_blocks] (unused entries -1) and num_tokens
+ * [n] of the listed sequences, ready to copy to the device.
+ */
+PA_API pa_status pa_block_manager_tables(pa_block_manager *m, const int64_t *seq_ids, int n,
+                                         int32_t *block_tables, int max_blocks,
+                                         int32_t *num_tokens);
+
+/*
  * Copies the device status word to *host_out after synchronising `stream`.
  * Returns PA_ERR_CUDA if the copy fails (for example after a sticky fault).
  */

@@ -32,7 +32,7 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -54,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     cc = nvcc()
     jobs = []
     for src in _sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         jobs.append((src, obj, [cc, *ARCH, *CFLAGS, *extra_flags, "-c", src, "-o", obj]))
 
     def run(job):

@@ -27,6 +27,9 @@ EXPORTS = (
     "pa_varlen_prefill_workspace_size", "pa_varlen_prefill", "pa_get_device_status",
     "pa_reset_device_status", "pa_set_timing_events", "pa_decode_static_scratch", "pa_decode_step",
     "pa_copy_blocks", "pa_varlen_encode",
+    "pa_block_manager_create", "pa_block_manager_destroy", "pa_block_manager_num_free",
+    "pa_block_manager_refcount", "pa_allocate_slots", "pa_free_sequence", "pa_share_prefix",
+    "pa_block_manager_tables",
 )
 STATIC_SCRATCH_BYTES = 24 << 20
 
@@ -71,6 +74,22 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_varlen_prefill.restype = i32
         L.pa_varlen_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                         i32, i32, f32, i32, vp, sz, vp, vp]
+        L.pa_block_manager_create.restype = vp
+        L.pa_block_manager_create.argtypes = [i32, i32, i32]
+        L.pa_block_manager_destroy.restype = None
+        L.pa_block_manager_destroy.argtypes = [vp]
+        L.pa_block_manager_num_free.restype = i32
+        L.pa_block_manager_num_free.argtypes = [vp]
+        L.pa_block_manager_refcount.restype = i32
+        L.pa_block_manager_refcount.argtypes = [vp, i32]
+        L.pa_allocate_slots.restype = i32
+        L.pa_allocate_slots.argtypes = [vp, i64, i32]
+        L.pa_free_sequence.restype = i32
+        L.pa_free_sequence.argtypes = [vp, i64]
+        L.pa_share_prefix.restype = i32
+        L.pa_share_prefix.argtypes = [vp, i64, i64, i32]
+        L.pa_block_manager_tables.restype = i32
+        L.pa_block_manager_tables.argtypes = [vp, vp, i32, vp, i32, vp]
         L.pa_varlen_encode.restype = i32
         L.pa_varlen_encode.argtypes = L.pa_varlen_prefill.argtypes
         L.pa_get_device_status.restype = i32
@@ -327,3 +346,53 @@ def decode_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale
         _opt(dev_status), _stream(stream))
     _check(rc, "pa_decode_static_scratch")
     return out
+
+
+class BlockManager:
+    """Host block pool (pa_block_manager_*): allocate_slots, free, shared prefixes,
+    and the int32 block tables / token counts the kernels consume."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16, max_blocks_per_seq: int = 4096):
+        self._L = load()
+        self._h = self._L.pa_block_manager_create(num_blocks, block_size, max_blocks_per_seq)
+        if not self._h:
+            raise ValueError("invalid block manager arguments")
+        self.num_blocks, self.block_size, self.max_blocks_per_seq = num_blocks, block_size, max_blocks_per_seq
+
+    def close(self):
+        if self._h:
+            self._L.pa_block_manager_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free(self) -> int:
+        return int(self._L.pa_block_manager_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(self._L.pa_block_manager_refcount(self._h, int(block)))
+
+    def allocate_slots(self, seq_id: int, num_new_tokens: int) -> int:
+        """Returns the status (OK, ERR_OUT_OF_RANGE when the pool is short, ...)."""
+        return int(self._L.pa_allocate_slots(self._h, int(seq_id), int(num_new_tokens)))
+
+    def free(self, seq_id: int) -> int:
+        return int(self._L.pa_free_sequence(self._h, int(seq_id)))
+
+    def share_prefix(self, parent_id: int, child_id: int, num_tokens: int) -> int:
+        return int(self._L.pa_share_prefix(self._h, int(parent_id), int(child_id), int(num_tokens)))
+
+    def tables(self, seq_ids, max_blocks: int):
+        """(block_tables int32 [n, max_blocks], num_tokens int32 [n]) as CPU tensors."""
+        ids = torch.tensor(list(seq_ids), dtype=torch.int64)
+        bt = torch.empty((ids.numel(), max_blocks), dtype=torch.int32)
+        nt = torch.empty(ids.numel(), dtype=torch.int32)
+        rc = self._L.pa_block_manager_tables(self._h, ids.data_ptr(), ids.numel(), bt.data_ptr(),
+                                             int(max_blocks), nt.data_ptr())
+        _check(rc, "pa_block_manager_tables")
+        return bt, nt
