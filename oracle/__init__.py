@@ -66,7 +66,9 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
+            # ORACLE_LIB points the tests at a deliberately broken build (the
+            # mutation tests check that the pins catch planted mistakes)
+            L = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
             vp, i32, i64, dp = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
             L.or_num_blocks_needed.restype = ctypes.c_longlong
             L.or_num_blocks_needed.argtypes = [ctypes.c_longlong, ctypes.c_longlong]
