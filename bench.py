@@ -376,17 +376,8 @@ def main():
     step_bytes = b["kv_unique"] + b["q"] + b["out"] + b["new_kv"] + b["meta"]
     total_s = r["total_ms"] / 1e3
     # whole job: units of all ranks over the slowest rank's time
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_s, float(step_bytes)], device="cuda")
-        tmax = t.clone()
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        tsum = t.clone()
-        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
-        total_s = float(tmax[0])
-        job_bytes = float(tsum[1]) * args.steps
-    else:
-        job_bytes = float(step_bytes) * args.steps
+    total_s, job_bytes = job_totals(total_s, float(step_bytes) * args.steps, world,
+                                    torch.device("cuda", local))
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -451,6 +442,21 @@ def main():
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def job_totals(seconds: float, bytes_done: float, world: int, device):
+    """(slowest rank's seconds, bytes of all ranks): the whole-job aggregate of a
+    replicated run.  No collective touches the data path; this one all-reduce
+    runs once, after the timed region."""
+    if world <= 1:
+        return seconds, bytes_done
+    import torch.distributed as dist
+    t = torch.tensor([seconds, bytes_done], dtype=torch.float64, device=device)
+    tmax = t.clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    tsum = t.clone()
+    dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+    return float(tmax[0]), float(tsum[1])
 
 
 def read_profile_traffic(config):
