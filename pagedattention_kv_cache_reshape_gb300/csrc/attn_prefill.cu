@@ -13,14 +13,14 @@
 // Work unit (one CTA): two M-tiles of 128 rows; a tile is POS consecutive
 // query positions x the G query heads of one kv-head, so each K/V tile is
 // loaded once for 2*POS positions of the whole group.  Keys come in tiles of
-// 64 (4 cache blocks) through a 3-deep TMA ring.
+// 128 (8 cache blocks); K and V of a tile take one slot each of a TMA ring.
 // Warp roles: warps 0-7 two softmax warpgroups (thread = row = TMEM lane of
 // its tile), warp 8 TMA producer, warp 9 TMEM owner and MMA issuer.
-//   S_t,j = Q_t K_j^T  -> TMEM (two buffers per tile)
-//   P_t,j = exp2(S_t,j * scale*log2e - m)  (bf16, shared memory, two buffers)
-//   O_t  += P_t,j V_j  -> TMEM (fp32)
-// The issuer runs QK of KV tile j for both M-tiles before PV of tile j-1, so
-// the tensor pipe has work while the softmax warpgroups turn S into P.
+//   S_t = Q_t K_j^T                         -> TMEM, fp32 (128 columns per tile)
+//   P_t = exp2(S_t * scale*log2e - m)       -> TMEM over S_t, bf16 pairs
+//   O_t += P_t V_j                          -> TMEM, fp32; A operand P_t read from TMEM
+// The two M-tiles alternate on the tensor pipe: while one softmax warpgroup
+// turns S into P, the products of the other tile run.
 // The running max is only raised (and O rescaled in TMEM) when a row's max
 // grows by more than 2^8; otherwise the stale max is kept, which changes no
 // result because l uses the same max.  Causal masking is a select on the
@@ -31,6 +31,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -40,12 +42,19 @@ namespace {
 constexpr int kB = kBlockSize;
 constexpr int BM = 128;               // rows per M-tile
 constexpr int kMT = 2;                // M-tiles per CTA, one softmax warpgroup each
-constexpr int BN = 64;                // keys per KV tile (4 cache blocks)
-constexpr int kStages = 3;            // K/V ring depth
+constexpr int BN = 128;               // keys per KV tile (8 cache blocks)
 constexpr int kBlocksPerTile = BN / kB;
+constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kProducerWarp = 4 * kMT;
 constexpr int kMmaWarp = kProducerWarp + 1;
-constexpr int kThreads = 32 * (kMmaWarp + 1);
+constexpr int kThreads = 32 * (4 * kMT + 4);  // the producer and MMA warps fill a warpgroup of their own
+// Register split: launched at 168 a thread (384 x 168 <= 64K), the producer /
+// MMA warpgroup drops to kRegsSide and the softmax warpgroups rise to
+// kRegsSoftmax; 128 * kRegsSide + 256 * kRegsSoftmax <= 384 * 168.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSide = 64;
+constexpr int kRegsSoftmax = 216;
+static_assert(128 * kRegsSide + 128 * kMT * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr int kPlanThreads = 512;
 constexpr int kTmemCols = 512;
 
@@ -53,15 +62,17 @@ struct PrefillParams {
     const int32_t *cu_seqlens_q;
     const int32_t *context_lens;
     const int32_t *block_tables;
-    const int2 *entries;       // (sequence, tile) per CTA
+    const int2 *entries;       // (sequence, CTA tile), most KV tiles first
     const int32_t *num_entries;
+    int32_t *next_item;        // work counter, zeroed by the plan kernel
     __nv_bfloat16 *out;
     int num_seqs;
     int total_q;
     int max_q_len;
     int num_heads;
+    int num_kv_heads;
     int group;       // q-heads per kv-head
-    int pos_shift;   // log2(query positions per tile) = log2(128 / group)
+    int pos_shift;   // log2(query positions per M-tile) = log2(128 / group)
     int max_blocks;
     int num_blocks;
     float scale_log2;
@@ -69,22 +80,49 @@ struct PrefillParams {
     int causal;      // 0: encode-only, every row sees the whole sequence
 };
 
+// KV tiles a CTA tile needs: keys up to its last row's position (causal) or
+// the whole sequence; 0 marks a tile the main kernel rejects.
+__device__ __forceinline__ int tile_kv_tiles(int q_len, int ctx, int tile, int cta_shift, int causal) {
+    const int i0 = tile << cta_shift;
+    const int nrows = min(1 << cta_shift, q_len - i0);
+    if (ctx <= 0 || q_len < 2 || q_len > ctx || nrows <= 0) return 0;
+    const int pos_last = causal ? ctx - q_len + i0 + nrows - 1 : ctx - 1;
+    return pos_last / BN + 1;
+}
+
 // ------------------------------------------------------------------ plan
-// One CTA: tiles per sequence with q_len >= 2, exclusive scan, one entry per
-// tile (the tile with the most keys first inside each sequence).
+// One CTA.  (1) The CTA tiles of every sequence with q_len >= 2, in sequence
+// order, into `scratch`; (2) a counting sort on the number of KV tiles, most
+// first, into `entries`, so the persistent CTAs take the longest work first
+// and finish together; (3) the work counter is reset.
+constexpr int kCostBuckets = 1024;
+constexpr int kPlanSmemTiles = 4096;          // tiles staged in shared memory (else in `scratch`)
+
 __global__ void __launch_bounds__(kPlanThreads)
-    prefill_plan_kernel(const int32_t *__restrict__ cu_seqlens_q, int num_seqs, int pos_shift,
-                        int2 *__restrict__ entries, int32_t *__restrict__ count, int capacity) {
+    prefill_plan_kernel(const int32_t *__restrict__ cu_seqlens_q, const int32_t *__restrict__ context_lens,
+                        int num_seqs, int cta_shift, int causal, int2 *__restrict__ scratch,
+                        int2 *__restrict__ entries, int32_t *__restrict__ count,
+                        int32_t *__restrict__ next_item, int capacity) {
     __shared__ int warp_tot[kPlanThreads / 32];
+    __shared__ int bucket[kCostBuckets];
+    __shared__ int2 tiles_s[kPlanSmemTiles];
+    __shared__ uint16_t cost_s[kPlanSmemTiles];
+    // the main kernel may start its prologue now; it waits for this grid
+    // before it reads the plan
+    grid_dependents_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int pos = 1 << pos_shift;
+    const bool in_smem = capacity <= kPlanSmemTiles;
+    int2 *tiles = in_smem ? tiles_s : scratch;
+    const int pos = 1 << cta_shift;
+    for (int b = tid; b < kCostBuckets; b += kPlanThreads) bucket[b] = 0;
     int running = 0;
     for (int base = 0; base < num_seqs; base += kPlanThreads) {
         const int s = base + tid;
-        int nt = 0;
+        int nt = 0, q_len = 0, ctx = 0;
         if (s < num_seqs) {
-            const int ql = __ldg(cu_seqlens_q + s + 1) - __ldg(cu_seqlens_q + s);
-            if (ql > 1) nt = (ql + pos - 1) >> pos_shift;
+            q_len = __ldg(cu_seqlens_q + s + 1) - __ldg(cu_seqlens_q + s);
+            ctx = __ldg(context_lens + s);
+            if (q_len > 1) nt = (q_len + pos - 1) >> cta_shift;
         }
         int incl = nt;
 #pragma unroll
@@ -99,358 +137,545 @@ __global__ void __launch_bounds__(kPlanThreads)
             if (w < warp) warp_off += warp_tot[w];
             chunk_tot += warp_tot[w];
         }
+        // bucket b holds the tiles with kCostBuckets-1-b KV tiles (the last
+        // bucket collects everything longer): ascending buckets = most work first
         const int first = running + warp_off + incl - nt;
-        for (int t = 0; t < nt; ++t)
-            if (first + t < capacity) entries[first + t] = make_int2(s, nt - 1 - t);
+        for (int t = 0; t < nt; ++t) {
+            if (first + t >= capacity) break;
+            const int c = tile_kv_tiles(q_len, ctx, t, cta_shift, causal);
+            const int b = kCostBuckets - 1 - min(c, kCostBuckets - 1);
+            tiles[first + t] = make_int2(s, t);
+            if (in_smem) cost_s[first + t] = (uint16_t)b;
+            atomicAdd(&bucket[b], 1);
+        }
         running += chunk_tot;
         __syncthreads();
     }
-    if (tid == 0) *count = running < capacity ? running : capacity;
+    const int total = running < capacity ? running : capacity;
+    // exclusive scan of the buckets, kCostBuckets / kPlanThreads per thread
+    constexpr int kPer = kCostBuckets / kPlanThreads;
+    int local[kPer], sum = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        local[k] = bucket[tid * kPer + k];
+        sum += local[k];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int off = incl - sum;
+    for (int w = 0; w < warp; ++w) off += warp_tot[w];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        bucket[tid * kPer + k] = off;
+        off += local[k];
+    }
+    __syncthreads();
+    for (int e = tid; e < total; e += kPlanThreads) {
+        const int2 v = tiles[e];
+        int b;
+        if (in_smem) {
+            b = cost_s[e];
+        } else {
+            const int q0 = __ldg(cu_seqlens_q + v.x);
+            const int c = tile_kv_tiles(__ldg(cu_seqlens_q + v.x + 1) - q0, __ldg(context_lens + v.x), v.y,
+                                        cta_shift, causal);
+            b = kCostBuckets - 1 - min(c, kCostBuckets - 1);
+        }
+        entries[atomicAdd(&bucket[b], 1)] = v;
+    }
+    if (tid == 0) {
+        *count = total;
+        *next_item = 0;
+    }
 }
 
 // ------------------------------------------------------------------ main kernel
+template <int D> struct Shape {
+    static constexpr int kDH = D / 64;                 // 64-column planes of a head
+    static constexpr int kQBytes = BM * D * 2;         // one M-tile of Q
+    static constexpr int kSlotBytes = BN * D * 2;      // K or V of one KV tile
+    static constexpr int kPlaneQ = BM * 128;           // one 64-column plane of Q
+    static constexpr int kPlaneKV = BN * 128;          // one 64-column plane of K or V
+    static constexpr int kBarBytes = 512;      // barriers, TMEM address, item slots
+    static constexpr int kFit = (int)((kSmemLimit - kMT * kQBytes - kBarBytes) / kSlotBytes);
+    static constexpr int kSlots = kFit < 8 ? kFit : 8;  // K/V ring depth
+    static constexpr size_t kSmem = (size_t)kMT * kQBytes + (size_t)kSlots * kSlotBytes + kBarBytes;
+    static_assert(kSlots >= 3, "the K/V ring needs at least three slots");
+    static_assert(kSmem <= kSmemLimit, "shared memory");
+};
+
+// One work item: CTA tile `entries[w / Hkv]` of kv-head w % Hkv.  `live` = 0
+// marks the end of the work; `valid` = 0 an item the kernel rejects.
+struct Item {
+    int s, g, q0, q_len, ctx, i0, nrows_all, pos_base, nkv, nb;
+    int valid, live;
+};
+constexpr int kItemSlots = 4;                 // items published ahead of their use
+
+__device__ __forceinline__ Item decode_item(const PrefillParams &p, int w) {
+    Item it;
+    const int e = w / p.num_kv_heads;
+    it.g = w - e * p.num_kv_heads;
+    const int2 ent = p.entries[e];
+    it.s = ent.x;
+    it.q0 = __ldg(p.cu_seqlens_q + it.s);
+    it.q_len = __ldg(p.cu_seqlens_q + it.s + 1) - it.q0;
+    it.ctx = __ldg(p.context_lens + it.s);
+    const int cta_shift = p.pos_shift + 1;             // kMT = 2 M-tiles per CTA tile
+    it.i0 = ent.y << cta_shift;
+    it.nrows_all = min(1 << cta_shift, it.q_len - it.i0);
+    it.pos_base = it.ctx - it.q_len + it.i0;
+    it.nkv = tile_kv_tiles(it.q_len, it.ctx, ent.y, cta_shift, p.causal);
+    it.nb = (it.ctx + kB - 1) / kB;
+    it.valid = it.nkv > 0 && (int64_t)it.ctx <= (int64_t)p.max_blocks * kB &&
+               it.q_len <= p.max_q_len && it.q0 >= 0 && it.q0 + it.q_len <= p.total_q;
+    it.live = 1;
+    return it;
+}
+
+// Persistent: one CTA per SM takes work items from a counter until none are
+// left.  The producer fetches the next item and starts its Q and K/V copies
+// while the tensor pipe and the softmax warpgroups still finish the current
+// one; the K/V ring, the TMEM buffers and every barrier carry over from item
+// to item, their phases counted by running totals that all roles keep alike.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
-    constexpr int kDH = D / 64;             // 64-column planes of a head
-    constexpr int kQBytes = BM * D * 2;     // one M-tile of Q
-    constexpr int kKVBytes = BN * D * 2;    // K (or V) of one KV tile
-    constexpr int kPBytes = BM * BN * 2;    // one P buffer
-    constexpr int kPlaneQ = BM * 128;       // one 64-column plane of Q or P
-    constexpr int kPlaneKV = BN * 128;      // one 64-column plane of K or V
+    using SH = Shape<D>;
+    constexpr int kDH = SH::kDH, kQBytes = SH::kQBytes, kSlotBytes = SH::kSlotBytes;
+    constexpr int kPlaneQ = SH::kPlaneQ, kPlaneKV = SH::kPlaneKV, kSlots = SH::kSlots;
     constexpr uint32_t kIdescQK = umma_idesc_bf16(BM, BN, 0);
     constexpr uint32_t kIdescPV = umma_idesc_bf16(BM, D, 1);
+    constexpr uint32_t kFull = 0xffffffffu;
 
     // all shared state is dynamic so the 1024-byte aligned tiles start at 0:
-    // Q[2] | (K,V) x kStages | P[2 tiles][2 buffers] | barriers
+    // Q[2] | K/V ring slots | barriers | item slots
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *q_s = smem;
     uint8_t *kv_s = smem + kMT * kQBytes;
-    uint8_t *p_s = kv_s + kStages * 2 * kKVBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(p_s + kMT * 2 * kPBytes);
-    uint64_t *q_full = bars;                       // 1
-    uint64_t *kv_full = q_full + 1;                // [kStages]
-    uint64_t *kv_empty = kv_full + kStages;        // [kStages]
-    uint64_t *s_full = kv_empty + kStages;         // [tile][buf]
-    uint64_t *p_full = s_full + 4;                 // [tile][buf]
-    uint64_t *p_free = p_full + 4;                 // [tile][buf]
-    uint64_t *drained = p_free + 4;                // 1: every product issued has completed
+    uint64_t *bars = reinterpret_cast<uint64_t *>(kv_s + kSlots * kSlotBytes);
+    uint64_t *q_full = bars;                       // Q of the item landed
+    uint64_t *q_empty = q_full + 1;                // every QK product of the item done
+    uint64_t *kv_full = q_empty + 1;               // [kSlots]: slot landed
+    uint64_t *kv_empty = kv_full + kSlots;         // [kSlots]: slot read by its products
+    uint64_t *s_full = kv_empty + kSlots;          // [tile]: S_t written
+    uint64_t *p_full = s_full + kMT;               // [tile]: P_t written (and O_t rescaled)
+    uint64_t *o_full = p_full + kMT;               // [tile]: last product of the item into O_t done
+    uint64_t *item_full = o_full + kMT;            // [kItemSlots]: item published
+    uint64_t *item_empty = item_full + kItemSlots; // [kItemSlots]: item read by every consumer
+    uint64_t *drained = item_empty + kItemSlots;   // every product issued has completed
     uint32_t &tmem_base_s = *reinterpret_cast<uint32_t *>(drained + 1);
-    int &abort_flag = *(reinterpret_cast<int *>(drained + 1) + 1);
+    Item *items = reinterpret_cast<Item *>(drained + 2);       // [kItemSlots]
+    static_assert((3 + 2 * kSlots + 3 * kMT + 2 * kItemSlots) * 8 + kItemSlots * sizeof(Item) <= SH::kBarBytes,
+                  "barrier area");
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.y;
-    if ((int)blockIdx.x >= __ldg(p.num_entries)) return;
-    const int2 ent = p.entries[blockIdx.x];
-    const int s = ent.x, tile = ent.y;
-    const int q0 = __ldg(p.cu_seqlens_q + s);
-    const int q_len = __ldg(p.cu_seqlens_q + s + 1) - q0;
-    const int ctx = __ldg(p.context_lens + s);
-    if (ctx <= 0 || (int64_t)ctx > (int64_t)p.max_blocks * kB || q_len < 2 || q_len > ctx ||
-        q_len > p.max_q_len || q0 < 0 || q0 + q_len > p.total_q) {
-        if (tid == 0) set_status(p.status, PA_ERR_OUT_OF_RANGE);
-        return;
-    }
-    const int POS = 1 << p.pos_shift;                  // query positions per M-tile
-    const int i0 = tile * kMT * POS;                   // first position of M-tile 0
-    const int nrows_all = min(kMT * POS, q_len - i0);  // valid positions of the CTA
-    if (nrows_all <= 0) return;
-    const int pos_base = ctx - q_len + i0;
-    const int pos_last = p.causal ? pos_base + nrows_all - 1 : ctx - 1;
-    const int nkv = pos_last / BN + 1;
-    const int nb = (ctx + kB - 1) / kB;
+    // the warp index broadcast from lane 0 is provably warp-uniform, so each
+    // role's branch is uniform and the MMA operands stay in uniform registers
+    // (computed per lane, a tcgen05.mma issue costs several times its run time)
+    const int tid = threadIdx.x, warp = __shfl_sync(kFull, tid >> 5, 0), lane = tid & 31;
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
         if (tid == 0) set_status(p.status, PA_ERR_CUDA);
         return;
     }
+    const int POS = 1 << p.pos_shift;                  // query positions per M-tile
 
     if (tid == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < kStages; ++i) {
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < kSlots; ++i) {
             mbar_init(kv_full + i, 1);
             mbar_init(kv_empty + i, 1);
         }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(s_full + i, 1);
-            mbar_init(p_full + i, BM);
-            mbar_init(p_free + i, 1);
+        for (int t = 0; t < kMT; ++t) {
+            mbar_init(s_full + t, 1);
+            mbar_init(p_full + t, BM);
+            mbar_init(o_full + t, 1);
+        }
+        for (int i = 0; i < kItemSlots; ++i) {
+            mbar_init(item_full + i, 1);
+            mbar_init(item_empty + i, 1 + 4 * kMT);      // the MMA warp and every softmax warp
         }
         mbar_init(drained, 1);
-        abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) tmem_alloc(&tmem_base_s, kTmemCols);
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tmap_q);
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // everything above overlaps the plan kernel; the plan (and every earlier
+    // write in the stream) is visible after this wait
+    grid_dependency_wait();
+    const int total = p.num_entries[0] * p.num_kv_heads;   // plain load: written by the plan grid
     const uint32_t tmem = tmem_base_s;
-    // TMEM columns: S[tile][buf] at (2 tile + buf) * BN, O[tile] at 4 BN + tile * D
-    auto s_col = [](int t, int b) { return (uint32_t)((2 * t + b) * BN); };
-    auto o_col = [](int t) { return (uint32_t)(4 * BN + t * D); };
+    // TMEM columns: S_t at t*BN (fp32, BN columns); P_t, bf16 pairs, over the
+    // first BN/2 columns of S_t; O_t at kMT*BN + t*D
+    auto s_col = [](int t) { return (uint32_t)(t * BN); };
+    auto o_col = [](int t) { return (uint32_t)(kMT * BN + t * D); };
+    // K/V ring: per item, entry n0 + 2j is K of KV tile j, n0 + 2j + 1 its V
+    auto slot_of = [](int n) { return n % kSlots; };
+    auto phase_of = [](int n) { return (uint32_t)((n / kSlots) & 1); };
+    // consumers: item `it` as the producer decoded it, with the read acknowledged
+    auto take_item = [&](int it, Item &I) -> bool {
+        if (!mbar_wait(item_full + it % kItemSlots, (uint32_t)((it / kItemSlots) & 1))) return false;
+        I = items[it % kItemSlots];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(item_empty + it % kItemSlots);
+        return true;
+    };
 
+    if (warp >= kProducerWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSide));
     if (warp == kProducerWarp) {
         // ================= TMA producer
         bool ok = true;
-        if (lane == 0) {
-            prefetch_tmap(&tmap_q);
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-            mbar_arrive_expect_tx(q_full, kMT * kQBytes);
-            for (int t = 0; t < kMT; ++t)
-                tma_load_4d(q_s + t * kQBytes, &tmap_q, 0, q0 + i0 + t * POS, g * p.group, 0, q_full);
-        }
-        // block ids, 32 per chunk (lane l holds block 32*chunk + l), one chunk ahead;
-        // past the sequence end (or invalid) the coordinate num_blocks is out of
-        // bounds and TMA fills zeros
-        const int32_t *bt = p.block_tables + (int64_t)s * p.max_blocks;
-        auto load_ids = [&](int chunk) {
-            const int lb = chunk * 32 + lane;
-            int coord = p.num_blocks;
-            if (lb < nb) {
-                const int32_t blk = __ldg(bt + lb);
-                if (blk >= 0 && blk < p.num_blocks) coord = blk;
-                else set_status(p.status, PA_ERR_OUT_OF_RANGE);
+        int n = 0, nq = 0;
+        // item `it`: the CTA's own first one, then ids from the counter; decoded
+        // once here and published one item ahead of its use, so no consumer
+        // and no Q copy waits on a fetch at an item boundary
+        auto publish = [&](int it, Item &I) -> bool {
+            bool okp = true;
+            int w = total;
+            if (lane == 0) {
+                if (it >= kItemSlots &&
+                    !mbar_wait(item_empty + it % kItemSlots, (uint32_t)(((it / kItemSlots) - 1) & 1)))
+                    okp = false;
+                else
+                    w = it == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.next_item, 1);
             }
-            return coord;
+            okp = __shfl_sync(kFull, okp ? 1 : 0, 0) != 0;
+            w = __shfl_sync(kFull, w, 0);
+            if (w < total) {
+                I = decode_item(p, w);
+            } else {
+                I = Item{};
+                I.live = 0;
+            }
+            if (lane == 0 && okp) {
+                items[it % kItemSlots] = I;
+                mbar_arrive(item_full + it % kItemSlots);
+            }
+            return okp;
         };
-        int ids_cur = load_ids(0), ids_next = load_ids(1), chunk_cur = 0;
-        for (int j = 0; j < nkv; ++j) {
-            const int stage = j % kStages;
-            if ((j * kBlocksPerTile) / 32 != chunk_cur) {
-                ids_cur = ids_next;
-                ++chunk_cur;
-                ids_next = load_ids(chunk_cur + 1);
+        Item I, I_next;
+        ok = publish(0, I);
+        for (int it = 0; ok && I.live; ++it, I = I_next) {
+            if (!publish(it + 1, I_next)) { ok = false; break; }
+            if (!I.valid) {
+                if (lane == 0) set_status(p.status, PA_ERR_OUT_OF_RANGE);
+                continue;
             }
-            if (lane == 0 && j >= kStages && !mbar_wait(kv_empty + stage, ((j / kStages) - 1) & 1)) ok = false;
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            // Q: its buffer is free once every QK product of the previous item completed
+            if (lane == 0) {
+                if (nq >= 1 && !mbar_wait(q_empty, (uint32_t)((nq - 1) & 1))) ok = false;
+                if (ok) {
+                    mbar_arrive_expect_tx(q_full, kMT * kQBytes);
+                    for (int t = 0; t < kMT; ++t)
+                        tma_load_4d(q_s + t * kQBytes, &tmap_q, 0, I.q0 + I.i0 + t * POS, I.g * p.group, 0, q_full);
+                }
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            int coords[kBlocksPerTile];
-            const int lb0 = (j * kBlocksPerTile) & 31;
-#pragma unroll
-            for (int b = 0; b < kBlocksPerTile; ++b) coords[b] = __shfl_sync(0xffffffffu, ids_cur, lb0 + b);
-            // lane 0 arms the barrier, then lanes (block, plane) issue one K and one V copy each
-            if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, 2 * kKVBytes);
-            __syncwarp();
-            if (lane < kBlocksPerTile * kDH) {
+            ++nq;
+            // block ids, 32 per chunk (lane l holds block 32*chunk + l), one chunk ahead;
+            // past the sequence end (or invalid) the coordinate num_blocks is out of
+            // bounds and TMA fills zeros
+            const int32_t *bt = p.block_tables + (int64_t)I.s * p.max_blocks;
+            auto load_ids = [&](int chunk) {
+                const int lb = chunk * 32 + lane;
+                int coord = p.num_blocks;
+                if (lb < I.nb) {
+                    const int32_t blk = __ldg(bt + lb);
+                    if (blk >= 0 && blk < p.num_blocks) coord = blk;
+                    else set_status(p.status, PA_ERR_OUT_OF_RANGE);
+                }
+                return coord;
+            };
+            int ids_cur = load_ids(0), ids_next = load_ids(1), chunk_cur = 0;
+            for (int j = 0; ok && j < I.nkv; ++j) {
+                if ((j * kBlocksPerTile) / 32 != chunk_cur) {
+                    ids_cur = ids_next;
+                    ++chunk_cur;
+                    ids_next = load_ids(chunk_cur + 1);
+                }
+                // lane (block b, plane dh) copies one 16-row box of K, then of V
                 const int b = lane / kDH, dh = lane % kDH;
-                int cb = coords[0];
-#pragma unroll
-                for (int u = 1; u < kBlocksPerTile; ++u) cb = b == u ? coords[u] : cb;
-                const uint32_t off = dh * kPlaneKV + b * (kB * 128);
-                uint8_t *ks = kv_s + stage * 2 * kKVBytes;
-                tma_load_5d(ks + off, &tmap_k, 0, 0, dh, g, cb, kv_full + stage);
-                tma_load_5d(ks + kKVBytes + off, &tmap_v, 0, 0, dh, g, cb, kv_full + stage);
+                const int cb = __shfl_sync(kFull, ids_cur, ((j * kBlocksPerTile) & 31) + (b & (kBlocksPerTile - 1)));
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int m = n + 2 * j + kv;
+                    if (lane == 0 && m >= kSlots && !mbar_wait(kv_empty + slot_of(m), phase_of(m) ^ 1u)) ok = false;
+                    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    if (lane == 0) mbar_arrive_expect_tx(kv_full + slot_of(m), kSlotBytes);
+                    __syncwarp();
+                    if (lane < kBlocksPerTile * kDH)
+                        tma_load_5d(kv_s + slot_of(m) * kSlotBytes + dh * kPlaneKV + b * (kB * 128),
+                                    kv ? &tmap_v : &tmap_k, 0, 0, dh, I.g, cb, kv_full + slot_of(m));
+                }
             }
+            n += 2 * I.nkv;
         }
-        if (!ok && lane == 0) {
-            set_status(p.status, PA_ERR_TIMEOUT);
-            abort_flag = 1;
-        }
+        if (!ok && lane == 0) set_status(p.status, PA_ERR_TIMEOUT);
         // every copy this CTA issued has landed before the CTA may exit
         if (lane == 0) {
-            mbar_wait(q_full, 0);
-            for (int j = nkv > kStages ? nkv - kStages : 0; j < nkv; ++j)
-                mbar_wait(kv_full + (j % kStages), (j / kStages) & 1);
+            if (nq >= 1) mbar_wait(q_full, (uint32_t)((nq - 1) & 1));
+            for (int m = n > kSlots ? n - kSlots : 0; m < n; ++m) mbar_wait(kv_full + slot_of(m), phase_of(m));
         }
     } else if (warp == kMmaWarp) {
-        // ================= MMA issuer (one thread): QK of KV tile j for both
-        // M-tiles, then PV of tile j-1, so the tensor pipe has work while the
-        // softmax warpgroups turn S into P
-        if (lane == 0) {
-            const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s), kv_addr = smem_u32(kv_s);
-            auto issue_qk = [&](int t, int j) {
-                const uint32_t k_addr = kv_addr + (j % kStages) * 2 * kKVBytes;
+        // ================= MMA issuer: the whole warp follows the schedule,
+        // lane 0 issues.  Tensor-pipe order, per KV tile j of an item:
+        //   PV_0(j)  QK_0(j+1)  PV_1(j)  QK_1(j+1)
+        // so the products of one M-tile run while the other tile's softmax
+        // turns S into P.  QK_t(j+1) (or QK_t(0) of the next item) overwrites
+        // the TMEM columns that PV_t(j) reads P_t from; the tensor pipe runs
+        // one thread's MMAs in issue order, so the read precedes the overwrite.
+        const bool leader = lane == 0;
+        const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(kv_s);
+        // descriptors: constant fields + (address >> 4) in bits 0..13
+        const uint64_t dq = umma_desc_sw128(q_addr, 16, 1024);
+        const uint64_t dk = umma_desc_sw128(kv_addr, 16, 1024);
+        const uint64_t dv = umma_desc_sw128(kv_addr, kPlaneKV, 1024);
+        auto issue_qk = [&](int t, int nk) {      // S_t = Q_t K^T, K in ring entry nk
+            const uint32_t ko = (uint32_t)slot_of(nk) * kSlotBytes;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off_q = t * kQBytes + (ks >> 2) * kPlaneQ + (ks & 3) * 32;
-                    const uint32_t off_k = (ks >> 2) * kPlaneKV + (ks & 3) * 32;
-                    umma_bf16(tmem + s_col(t, j & 1), umma_desc_sw128(q_addr + off_q, 16, 1024),
-                              umma_desc_sw128(k_addr + off_k, 16, 1024), kIdescQK, ks > 0);
-                }
-            };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t v_addr = kv_addr + (j % kStages) * 2 * kKVBytes + kKVBytes;
-                const uint32_t pb = p_addr + (2 * t + (j & 1)) * kPBytes;
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off = (ks >> 2) * kPlaneKV + (ks & 3) * 32;
+                const uint32_t offq = t * kQBytes + (ks >> 2) * kPlaneQ + (ks & 3) * 32;
+                if (leader)
+                    umma_bf16(tmem + s_col(t), dq + (offq >> 4), dk + ((ko + off) >> 4), kIdescQK, ks > 0);
+            }
+        };
+        auto issue_pv = [&](int t, int nv, bool first) {   // O_t (+)= P_t V, V in ring entry nv
+            const uint32_t vo = (uint32_t)slot_of(nv) * kSlotBytes;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t off_p = (kk >> 2) * kPlaneQ + (kk & 3) * 32;
-                    umma_bf16(tmem + o_col(t), umma_desc_sw128(pb + off_p, 16, 1024),
-                              umma_desc_sw128(v_addr + kk * 2048, kPlaneKV, 1024), kIdescPV,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-                }
-            };
-            auto pv_step = [&](int j) -> bool {   // PV of KV tile j for both M-tiles
+            for (int kk = 0; kk < BN / 16; ++kk)
+                if (leader)
+                    umma_bf16_tmem_a(tmem + o_col(t), tmem + s_col(t) + kk * 8, dv + ((vo + kk * 2048) >> 4),
+                                     kIdescPV, (!first || kk > 0) ? 1u : 0u);
+        };
+        auto commit = [&](uint64_t *bar) {
+            if (leader) umma_commit(bar);
+        };
+        bool ok = true;
+        int n = 0, J = 0, nq = 0;
+        for (int it = 0; ok; ++it) {
+            Item I;
+            if (!take_item(it, I)) { ok = false; break; }
+            if (!I.live) break;
+            if (!I.valid) continue;
+            const int nkv = __shfl_sync(kFull, I.nkv, 0);
+            if (!mbar_wait(q_full, (uint32_t)(nq & 1)) || !mbar_wait(kv_full + slot_of(n), phase_of(n))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int t = 0; t < kMT; ++t) {
+                issue_qk(t, n);
+                commit(s_full + t);
+            }
+            if (nkv == 1) commit(q_empty);
+            commit(kv_empty + slot_of(n));
+            for (int j = 0; j < nkv; ++j) {
+                const bool next = j + 1 < nkv;
+                const int nv = n + 2 * j + 1, nk = n + 2 * j + 2;
+                if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv))) { ok = false; break; }
                 for (int t = 0; t < kMT; ++t) {
-                    if (!mbar_wait(p_full + 2 * t + (j & 1), (j >> 1) & 1)) return false;
+                    if (!mbar_wait(p_full + t, (uint32_t)((J + j) & 1))) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv(t, j);
-                    umma_commit(p_free + 2 * t + (j & 1));
+                    issue_pv(t, nv, j == 0);
+                    if (next) {
+                        if (t == 0 && !mbar_wait(kv_full + slot_of(nk), phase_of(nk))) { ok = false; break; }
+                        tc_fence_after();
+                        issue_qk(t, nk);
+                        commit(s_full + t);
+                    } else {
+                        commit(o_full + t);
+                    }
                 }
-                umma_commit(kv_empty + (j % kStages));
-                return true;
-            };
-            bool ok = mbar_wait(q_full, 0);
-            int pv_issued = 0;
-            for (int j = 0; ok && j < nkv; ++j) {
-                if (!mbar_wait(kv_full + (j % kStages), (j / kStages) & 1)) { ok = false; break; }
-                tc_fence_after();
-                for (int t = 0; t < kMT; ++t) {
-                    issue_qk(t, j);
-                    umma_commit(s_full + 2 * t + (j & 1));
-                }
-                if (j >= 1) {
-                    if (!pv_step(j - 1)) { ok = false; break; }
-                    ++pv_issued;
+                if (!ok) break;
+                commit(kv_empty + slot_of(nv));
+                if (next) {
+                    commit(kv_empty + slot_of(nk));
+                    if (j + 2 == nkv) commit(q_empty);    // the item's last QK products
                 }
             }
-            if (ok) {
-                if (pv_step(nkv - 1)) ++pv_issued;
-                else ok = false;
-            }
-            if (!ok) {
-                set_status(p.status, PA_ERR_TIMEOUT);
-                abort_flag = 1;
-            }
-            // drain: everything issued must finish before TMEM is released
-            umma_commit(drained);
-            mbar_wait(drained, 0);
-            (void)pv_issued;
+            n += 2 * nkv;
+            J += nkv;
+            ++nq;
         }
+        if (!ok && leader) set_status(p.status, PA_ERR_TIMEOUT);
+        // drain: everything issued must finish before TMEM is released
+        commit(drained);
+        mbar_wait(drained, 0);
         __syncwarp();
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ================= softmax warpgroup t: thread r owns row r of M-tile t
         const int t = warp >> 2;
         const int r = tid & (BM - 1);
         const int h_local = r >> p.pos_shift;
-        const int i = t * POS + (r & (POS - 1));          // position index within the CTA
-        const bool row_valid = i < nrows_all;
-        // last visible key of this row: its position (causal) or the sequence end
-        const int pos = p.causal ? pos_base + (row_valid ? i : nrows_all - 1) : ctx - 1;
-        const int first_pos = p.causal ? pos_base + t * POS : ctx - 1;   // smallest pos of the tile
+        const int i = t * POS + (r & (POS - 1));          // position index within the CTA tile
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const int t_tail = ctx & (kB - 1);          // valid tokens in the last block (0 = full)
-        const int lb_last = (ctx - 1) / kB;
-        float m = -INFINITY, l = 0.f;
+        const float sl2 = p.scale_log2;
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            const int b = j & 1;
-            if (!mbar_wait(s_full + 2 * t + b, (j >> 1) & 1)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t raw[BN / 32][32];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_addr + s_col(t, b) + 32 * c, raw[c]);
-            tmem_wait_ld();
-            float sv[BN];
-            float mx = -INFINITY;
-            const int key0 = j * BN;
-            const bool diag = key0 + BN - 1 > first_pos;   // a key past some row of this tile
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float x = __uint_as_float(raw[c][e]) * p.scale_log2;
-                    const float v = (!diag || key0 + 32 * c + e <= pos) ? x : -INFINITY;
-                    sv[32 * c + e] = v;
-                    mx = fmaxf(mx, v);
-                }
-            const float m_new = fmaxf(m, mx);
-            // the running max moves only when it grows by more than 2^8
-            const bool need = (j == 0) || m_new > m + 8.f;
-            const float m_use_new = need ? m_new : m;
-            const float m_use = m_use_new == -INFINITY ? 0.f : m_use_new;
-            float lsum = 0.f;
-            uint32_t pw[BN / 2];
-#pragma unroll
-            for (int u = 0; u < BN / 2; ++u) {
-                const float p0 = fast_exp2(sv[2 * u] - m_use);
-                const float p1 = fast_exp2(sv[2 * u + 1] - m_use);
-                lsum += p0 + p1;
-                pw[u] = pack_bf16x2(p0, p1);
-            }
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // O must hold every earlier product before it is rescaled: wait
-                // for the commit of PV(j-1) on its P buffer (that barrier is at
-                // most one phase ahead of this wait, so its parity is exact;
-                // a commit also covers every earlier product)
-                if (!mbar_wait(p_free + 2 * t + ((j - 1) & 1), ((j - 1) >> 1) & 1)) { ok = false; break; }
+        int n = 0, J = 0, no = 0;
+        for (int it = 0; ok; ++it) {
+            Item I;
+            if (!take_item(it, I)) { ok = false; break; }
+            if (!I.live) break;
+            if (!I.valid) continue;
+            const bool row_valid = i < I.nrows_all;
+            // last visible key of this row: its position (causal) or the sequence end
+            const int pos = p.causal ? I.pos_base + (row_valid ? i : I.nrows_all - 1) : I.ctx - 1;
+            const int first_pos = p.causal ? I.pos_base + t * POS : I.ctx - 1;   // smallest pos of the tile
+            const int t_tail = I.ctx & (kB - 1);        // valid tokens in the last block (0 = full)
+            const int lb_last = (I.ctx - 1) / kB;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < I.nkv; ++j) {
+                if (!mbar_wait(s_full + t, (uint32_t)((J + j) & 1))) { ok = false; break; }
                 tc_fence_after();
-                const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-                l *= alpha;
+                const int key0 = j * BN;
+                const bool diag = key0 + BN - 1 > first_pos;    // a key past some row of this tile
+                // P = 2^(S * scale*log2e - m), bf16 pairs in registers; the first
+                // tile takes its own max (key 0 is visible to every row), later
+                // tiles run with the running max first: P stays <= 2^8 unless the
+                // tile's max exceeds it by more than 8, and then (rarely) the row
+                // moves its max, rescales O and redoes the tile from S, which is
+                // intact in TMEM until P is stored over it
+                uint32_t pk[BN / 2];
+                float lsum;
+                for (;;) {
+                    uint32_t sr[BN / 32][32];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
+                    for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_addr + s_col(t) + 32 * c, sr[c]);
                     tmem_wait_ld();
+                    if (diag) {
+                        const int lim = pos - key0;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(lane_addr + o_col(t) + 32 * c, o);
+                        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (32 * c + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
+                    }
+                    if (j == 0 && m == -INFINITY) {
+                        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                mx0 = fmax3(mx0, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                                mx1 = fmax3(mx1, __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
+                            }
+                        const float m0 = fmaxf(mx0, mx1) * sl2;
+                        m = m0 == -INFINITY ? 0.f : m0;
+                    }
+                    float ls0 = 0.f, ls1 = 0.f, mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                    for (int u = 0; u < BN / 2; ++u) {
+                        const float s0 = __uint_as_float(sr[u >> 4][(2 * u) & 31]);
+                        const float s1 = __uint_as_float(sr[u >> 4][(2 * u + 1) & 31]);
+                        if (u & 1) mx1 = fmax3(mx1, s0, s1);
+                        else mx0 = fmax3(mx0, s0, s1);
+                        const float p0 = fast_exp2(fmaf(s0, sl2, -m));
+                        const float p1 = fast_exp2(fmaf(s1, sl2, -m));
+                        ls0 += p0;
+                        ls1 += p1;
+                        pk[u] = pack_bf16x2(p0, p1);
+                    }
+                    lsum = ls0 + ls1;
+                    const float m_tile = fmaxf(mx0, mx1) * sl2;
+                    const bool need = m_tile > m + 8.f;
+                    if (!__any_sync(kFull, need)) break;
+                    const float m_new = need ? m_tile : m;
+                    const float alpha = fast_exp2(m - m_new);
+                    l *= alpha;
+                    // PV_t(j-1) completed before S_t(j) was committed, so O_t is final here
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(lane_addr + o_col(t) + 32 * c, o);
+                    }
+                    m = m_new;
+                }
+                // P_t over the first BN/2 columns of S_t
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c)
+                    tmem_st32(lane_addr + s_col(t) + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * c));
+                l += lsum;
+                // value rows past the context end inside the last block -> zero
+                // (warpgroup 0 only; its p_full arrival orders the writes before
+                // every product that reads this V tile)
+                if (t == 0 && t_tail != 0) {
+                    const int bb = lb_last - j * kBlocksPerTile;
+                    if (bb >= 0 && bb < kBlocksPerTile) {
+                        const int nv = n + 2 * j + 1;
+                        if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv))) { ok = false; break; }
+                        uint8_t *vs = kv_s + slot_of(nv) * kSlotBytes;
+                        const int rows_zero = kB - t_tail;
+                        const int n16 = kDH * rows_zero * 8;
+                        for (int u = r; u < n16; u += BM) {
+                            const int dh = u / (rows_zero * 8);
+                            const int rem = u - dh * rows_zero * 8;
+                            const int tok = t_tail + (rem >> 3);
+                            *reinterpret_cast<uint4 *>(vs + dh * kPlaneKV + (bb * kB + tok) * 128 + (rem & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                    }
                 }
                 tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_full + t);
             }
-            m = m_use_new;
-            // value rows past the context end inside the last block -> zero
-            // (warpgroup 0 only; its p_full arrival orders the writes before
-            // every product of this KV tile)
-            if (t == 0 && t_tail != 0) {
-                const int bb = lb_last - j * kBlocksPerTile;
-                if (bb >= 0 && bb < kBlocksPerTile) {
-                    if (!mbar_wait(kv_full + (j % kStages), (j / kStages) & 1)) { ok = false; break; }
-                    uint8_t *vs = kv_s + (j % kStages) * 2 * kKVBytes + kKVBytes;
-                    const int rows_zero = kB - t_tail;
-                    const int n16 = kDH * rows_zero * 8;
-                    for (int u = r; u < n16; u += BM) {
-                        const int dh = u / (rows_zero * 8);
-                        const int rem = u - dh * rows_zero * 8;
-                        const int tok = t_tail + (rem >> 3);
-                        *reinterpret_cast<uint4 *>(vs + dh * kPlaneKV + (bb * kB + tok) * 128 + (rem & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-            }
-            // the P buffer is free once the product two tiles back has read it
-            if (j >= 2 && !mbar_wait(p_free + 2 * t + b, ((j >> 1) - 1) & 1)) { ok = false; break; }
-            uint8_t *pbuf = p_s + (2 * t + b) * kPBytes;
-#pragma unroll
-            for (int q4 = 0; q4 < BN / 8; ++q4) {
-                const int kt = 8 * q4;                          // first key of this 16-byte chunk
-                const int chunk = (kt & 63) >> 3;
-                uint8_t *dst = pbuf + (kt >> 6) * kPlaneQ + r * 128 + ((chunk ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
-            }
-            l += lsum;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(p_full + 2 * t + b);
-        }
-        // ---- epilogue: O / l -> bf16 rows of out, after the commit of the last product
-        if (ok && mbar_wait(p_free + 2 * t + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1)) {
+            if (!ok) break;
+            // ---- epilogue: O / l -> bf16 rows of out, after the last product into O_t.
+            // The next item's first product into O_t waits for this warpgroup's
+            // next P, so these TMEM loads complete before O_t is overwritten.
+            if (!mbar_wait(o_full + t, (uint32_t)(no & 1))) { ok = false; break; }
             tc_fence_after();
             const float inv = 1.f / l;
-            __nv_bfloat16 *dst = p.out + ((int64_t)(q0 + i0 + i) * p.num_heads +
-                                          (int64_t)g * p.group + h_local) * D;
+            __nv_bfloat16 *dst = p.out + ((int64_t)(I.q0 + I.i0 + i) * p.num_heads +
+                                          (int64_t)I.g * p.group + h_local) * D;
+            uint32_t o[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
-                tmem_wait_ld();
-                if (row_valid) {
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_addr + o_col(t) + 32 * c, o[c]);
+            tmem_wait_ld();
+            if (row_valid) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint32_t *v8 = o[c] + 8 * q4;
                         uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+                        v.x = pack_bf16x2(__uint_as_float(v8[0]) * inv, __uint_as_float(v8[1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(v8[2]) * inv, __uint_as_float(v8[3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(v8[4]) * inv, __uint_as_float(v8[5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(v8[6]) * inv, __uint_as_float(v8[7]) * inv);
                         *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = v;
                     }
-                }
             }
-        } else if (!ok) {
-            if (r == 0) set_status(p.status, PA_ERR_TIMEOUT);
-            abort_flag = 1;
+            n += 2 * I.nkv;
+            J += I.nkv;
+            ++no;
         }
+        if (!ok && r == 0) set_status(p.status, PA_ERR_TIMEOUT);
     }
 
     tc_fence_before();
@@ -500,18 +725,32 @@ int log2_exact(int v) {
 
 template <int D>
 cudaError_t launch_main(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                        const PrefillParams &prm, int grid_x, int num_kv_heads, cudaStream_t stream) {
-    const size_t smem = (size_t)kMT * BM * D * 2 + (size_t)kStages * 2 * BN * D * 2 +
-                        (size_t)kMT * 2 * BM * BN * 2 + 256;
+                        const PrefillParams &prm, int grid, cudaStream_t stream) {
+    const size_t smem = Shape<D>::kSmem;
     auto kern = prefill_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(grid_x, num_kv_heads), kThreads, smem, stream>>>(mq, mk, mv, prm);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(kThreads), smem, stream, mq, mk, mv, prm);
 }
+
+int sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// CTA tiles a batch can produce: at least 2 * 8 positions per tile (G <= 16)
+// plus one partial tile per sequence.
+size_t plan_capacity(int num_seqs, int total_q) { return (size_t)total_q / 8 + num_seqs + 1; }
 
 }  // namespace
 
@@ -525,8 +764,8 @@ bool prefill_tc_supported(const AttnArgs &a) {
 }
 
 size_t prefill_workspace(int num_seqs, int total_q) {
-    // plan entries: at most total_q / 8 + num_seqs tiles (8 = fewest positions per tile)
-    return align_up(sizeof(int2) * ((size_t)total_q / 8 + num_seqs + 1) + 16, 256);
+    // [count, work counter, pad] | scratch tiles | sorted tiles
+    return align_up(16 + 2 * sizeof(int2) * plan_capacity(num_seqs, total_q), 256);
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspace_bytes,
@@ -534,11 +773,13 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     const int G = a.num_heads / a.num_kv_heads;
     const int pos = BM / G;
     const int pos_shift = log2_exact(pos);
-    const int cta_shift = pos_shift + 1;          // kMT = 2 M-tiles of `pos` positions per CTA
-    const int capacity = a.total_q / (kMT * pos) + a.num_seqs;
+    const int cta_shift = pos_shift + 1;          // kMT = 2 M-tiles of `pos` positions per CTA tile
+    const size_t capacity = plan_capacity(a.num_seqs, a.total_q);
     if (workspace_bytes < prefill_workspace(a.num_seqs, a.total_q)) return cudaErrorInvalidValue;
     int32_t *count = static_cast<int32_t *>(workspace);
-    int2 *entries = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + 16);
+    int32_t *next_item = count + 1;
+    int2 *scratch = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + 16);
+    int2 *entries = scratch + capacity;
 
     CUtensorMap mq, mk, mv;
     if (make_q_map(&mq, a.q, a.total_q, a.num_heads, a.head_dim, pos, G) != CUDA_SUCCESS ||
@@ -546,8 +787,9 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
         make_kv_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
 
-    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens_q, a.num_seqs, cta_shift, entries,
-                                                         count, capacity);
+    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens_q, a.context_lens, a.num_seqs, cta_shift,
+                                                         a.causal, scratch, entries, count, next_item,
+                                                         (int)capacity);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -557,11 +799,13 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     prm.block_tables = a.block_tables;
     prm.entries = entries;
     prm.num_entries = count;
+    prm.next_item = next_item;
     prm.out = static_cast<__nv_bfloat16 *>(a.out);
     prm.num_seqs = a.num_seqs;
     prm.total_q = a.total_q;
     prm.max_q_len = a.max_q_len;
     prm.num_heads = a.num_heads;
+    prm.num_kv_heads = a.num_kv_heads;
     prm.group = G;
     prm.pos_shift = pos_shift;
     prm.max_blocks = a.max_blocks;
@@ -569,8 +813,11 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.status = a.status;
     prm.causal = a.causal;
-    return a.head_dim == 64 ? launch_main<64>(mq, mk, mv, prm, capacity, a.num_kv_heads, stream)
-                            : launch_main<128>(mq, mk, mv, prm, capacity, a.num_kv_heads, stream);
+    // persistent: one CTA per SM, never more CTAs than work items
+    const size_t items = capacity * (size_t)a.num_kv_heads;
+    const int grid = (int)(items < (size_t)sm_count() ? items : (size_t)sm_count());
+    return a.head_dim == 64 ? launch_main<64>(mq, mk, mv, prm, grid, stream)
+                            : launch_main<128>(mq, mk, mv, prm, grid, stream);
 }
 
 }  // namespace pa
