@@ -52,6 +52,12 @@ constexpr int kMaxSeqs = 16384;     // prefix of all sequences kept in shared me
 constexpr int kPartialCtas = 512;   // partial slots reserved for CTA boundaries
 constexpr int kPlanThreads = 256;
 constexpr int kSmemBudget = 227 * 1024;
+// Per-SM rates for splitting the SMs between the decode rows and a concurrent
+// prefill kernel (measured on GB300): the decode kernel streams at most about
+// 82 GB/s from one SM; the tcgen05 prefill kernel sustains about 5.9 TFLOP/s
+// per SM on causal chunks.
+constexpr double kDecodeBytesPerSmNs = 82.0;
+constexpr double kPrefillFlopsPerSmNs = 5900.0;
 
 struct __align__(16) StreamEntry {
     int32_t seq;
@@ -78,6 +84,8 @@ struct DecodeParams {
     int group;     // q-heads per kv-head
     int qh;        // q-heads per CTA = kvh * group
     int nhg;       // kv-head groups
+    const int32_t *active;     // CTAs that take a slice (written by the plan; the rest exit)
+    int shared_sms;            // 1: `active` is set (a prefill kernel shares the SMs); 0: all CTAs
     int num_stages;
     int tma_heads; // kv-heads per TMA op (kvh, or 1 with the per-head map)
     float scale_log2;
@@ -103,25 +111,51 @@ struct KvWriteJob {
     int64_t pool_slots;
 };
 
+// How many of the decode kernel's CTAs take a slice.  Alone on the GPU,
+// every CTA does.  Beside the tensor-core prefill of the same batch (which
+// runs concurrently and takes over the SMs the decode kernel leaves), the
+// SMs are split by estimated work: decode blocks at the per-SM streaming
+// rate against the causal (query, key) pairs of the prefill rows at the
+// per-SM tensor rate, both measured on GB300.
+struct DecodeSplit {
+    int32_t *active;
+    int grid;          // CTAs the decode kernel is launched with
+    int share;         // 1: a prefill kernel runs beside this one
+    int causal;
+    double block_ns;   // SM-nanoseconds per decode block of all kv-heads
+    double pair_ns;    // SM-nanoseconds per causal (query row, key) pair of all heads
+};
+
 // ------------------------------------------------------------------ plan
+// kShare: the batch also has prefill chunks (the extra CTA plans them and CTA
+// 0 sets the SM split); decode-only calls run the plain instantiation.
+template <bool kShare>
 __global__ void __launch_bounds__(kPlanThreads)
     decode_plan_kernel(const int32_t *__restrict__ context_lens,
                        const int32_t *__restrict__ cu_seqlens_q,
                        const int32_t *__restrict__ block_tables, int num_seqs, int max_blocks,
                        int num_blocks, int total_q, int32_t *__restrict__ prefix,
-                       StreamEntry *__restrict__ stream, int32_t *status, const KvWriteJob job) {
-    extern __shared__ int32_t pref_s[];  // [num_seqs + 1], then cu_new [num_seqs + 1]
+                       StreamEntry *__restrict__ stream, int32_t *status, const KvWriteJob job,
+                       const DecodeSplit split, const PrefillPlanJob prefill) {
+    extern __shared__ __align__(16) int32_t pref_s[];  // [num_seqs + 1], then cu_new [num_seqs + 1]
     __shared__ int32_t warp_tot[kPlanThreads / 32];
+    __shared__ double pair_tot[kPlanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();      // inputs may come from the previous kernel
     grid_dependents_launch();    // the decode kernel may start its prologue
+    // with prefill chunks in the batch, the last CTA builds their work list
+    const int dgrid = (int)gridDim.x - (kShare ? 1 : 0);   // CTAs of the decode plan proper
+    if (kShare && (int)blockIdx.x == dgrid) {
+        prefill_plan_block(prefill, reinterpret_cast<uint8_t *>(pref_s));
+        return;
+    }
     if (job.total_new > 0) {
         // ---- the step's cache write: one warp per new token
         int32_t *cu_s = pref_s + num_seqs + 1;
         for (int i = tid; i <= num_seqs; i += kPlanThreads) cu_s[i] = __ldg(job.cu_new + i);
         __syncthreads();
         const int warps = kPlanThreads / 32;
-        for (int t = blockIdx.x * warps + warp; t < job.total_new; t += gridDim.x * warps) {
+        for (int t = blockIdx.x * warps + warp; t < job.total_new; t += dgrid * warps) {
             int64_t slot = -1;
             if (lane == 0) {
                 int lo = 0, hi = num_seqs;  // last s with cu_new[s] <= t
@@ -156,6 +190,7 @@ __global__ void __launch_bounds__(kPlanThreads)
         __syncthreads();
     }
     int running = 0;
+    double pairs = 0.0;   // causal (query, key) pairs of this thread's prefill rows
     for (int base = 0; base < num_seqs; base += kPlanThreads) {
         const int s = base + tid;
         int nb = 0;
@@ -164,6 +199,9 @@ __global__ void __launch_bounds__(kPlanThreads)
             const int q1 = cu_seqlens_q ? __ldg(cu_seqlens_q + s + 1) : s + 1;
             const int q_len = q1 - q0;
             const int ctx = __ldg(context_lens + s);
+            if (kShare && q_len >= 2 && q_len <= ctx)
+                pairs += split.causal ? (double)q_len * (ctx - q_len) + 0.5 * (double)q_len * (q_len + 1)
+                                      : (double)q_len * ctx;
             if (q0 < 0 || q1 < q0 || q1 > total_q) {
                 if (blockIdx.x == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
             } else if (q_len == 1) {
@@ -193,11 +231,32 @@ __global__ void __launch_bounds__(kPlanThreads)
         __syncthreads();
     }
     if (tid == 0) pref_s[num_seqs] = running;
+    if (kShare && blockIdx.x == 0) {
+        // CTAs of the decode kernel that take a slice
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) pairs += __shfl_xor_sync(0xffffffffu, pairs, off);
+        if (lane == 0) pair_tot[warp] = pairs;
+        __syncthreads();
+        if (tid == 0) {
+            int act = split.grid;
+            {
+                double pf = 0.0;
+                for (int w = 0; w < kPlanThreads / 32; ++w) pf += pair_tot[w];
+                const double dec = (double)running * split.block_ns;
+                pf *= split.pair_ns;
+                if (pf > 0.0 && dec > 0.0) {
+                    act = (int)llrint(split.grid * dec / (dec + pf));
+                    act = act < 1 ? 1 : (act > split.grid ? split.grid : act);
+                }
+            }
+            *split.active = act;
+        }
+    }
     __syncthreads();
     const int T = running;
     if (blockIdx.x == 0)
         for (int s = tid; s <= num_seqs; s += kPlanThreads) prefix[s] = pref_s[s];
-    for (int b = blockIdx.x * kPlanThreads + tid; b < T; b += gridDim.x * kPlanThreads) {
+    for (int b = blockIdx.x * kPlanThreads + tid; b < T; b += dgrid * kPlanThreads) {
         int lo = 0, hi = num_seqs;  // last s with pref_s[s] <= b
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -268,7 +327,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
     const int S = p.num_seqs;
     const int64_t T = __ldg(p.prefix + S);
     const int64_t NV = T * p.nhg;
-    const int64_t P = gridDim.x;
+    const int64_t P = p.shared_sms ? min((int64_t)gridDim.x, (int64_t)__ldg(p.active)) : (int64_t)gridDim.x;
+    if ((int64_t)blockIdx.x >= P) return;   // this SM is left to the prefill kernel
     const int64_t lo = cta_slice_begin(blockIdx.x, NV, P);
     const int64_t hi = cta_slice_begin(blockIdx.x + 1, NV, P);
     const int nloc = (int)(hi - lo);
@@ -525,7 +585,7 @@ __global__ void __launch_bounds__(256)
     const int hg = vs / S, s = vs % S;
     const int64_t T = __ldg(p.prefix + S);
     const int64_t NV = T * p.nhg;
-    const int64_t P = num_ctas;
+    const int64_t P = p.shared_sms ? min((int64_t)num_ctas, (int64_t)__ldg(p.active)) : (int64_t)num_ctas;
     const int64_t b0 = __ldg(p.prefix + s), b1 = __ldg(p.prefix + s + 1);
     if (b1 == b0) return;
     const int64_t c0 = cta_of(hg * T + b0, NV, P);
@@ -617,14 +677,15 @@ Layout decode_layout(int num_heads, int num_kv_heads) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WorkspaceLayout {
-    size_t prefix, stream, part_ml, part_o, total;
+    size_t prefix, active, stream, part_ml, part_o, total;
 };
 
 WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_blocks) {
     WorkspaceLayout w;
     const size_t slots_heads = ((size_t)num_seqs + kPartialCtas) * num_heads;
     w.prefix = 0;
-    w.stream = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 256);
+    w.active = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 16);
+    w.stream = align_up(w.active + sizeof(int32_t), 256);
     w.part_ml = align_up(w.stream + sizeof(StreamEntry) * (size_t)num_seqs * max_blocks, 256);
     w.part_o = align_up(w.part_ml + sizeof(float) * 2 * slots_heads, 256);
     w.total = align_up(w.part_o + sizeof(float) * (size_t)head_dim * slots_heads, 256);
@@ -633,7 +694,8 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
 
 template <int D>
 cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtensorMap &mk,
-                        const CUtensorMap &mv, int grid, cudaStream_t stream, bool timed) {
+                        const CUtensorMap &mv, int grid, cudaStream_t stream, bool timed,
+                        const std::function<cudaError_t()> *between) {
     const int kv_tile = prm.kvh * kB * D * 2;
     const int stage_bytes = (int)align_up(2 * kv_tile + prm.qh * D * 2, 1024);
     const size_t smem = 1024 + (size_t)prm.num_stages * (stage_bytes + sizeof(StageHeader) + 16);
@@ -644,6 +706,10 @@ cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtens
     e = launch_dependent(kern, dim3(grid), dim3(32 * (prm.kvh + 1)), smem, stream, mk, mv, prm);
     if (timed) timing_end(stream);
     if (e != cudaSuccess) return e;
+    if (between) {
+        e = (*between)();
+        if (e != cudaSuccess) return e;
+    }
     const int warps = prm.nhg * prm.num_seqs * prm.qh;
     return launch_dependent(split_decode_reduce_kernel<D>, dim3((warps + 7) / 8), dim3(256), 0, stream,
                             prm, grid);
@@ -677,7 +743,10 @@ size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max
 }
 
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                                cudaStream_t stream, bool timed, const KvWriteArgs *write) {
+                                cudaStream_t stream, bool timed, const KvWriteArgs *write,
+                                const PrefillPlanJob *prefill,
+                                const std::function<cudaError_t()> *between) {
+    const bool share_sms = prefill != nullptr;
     if (a.num_seqs == 0) return cudaSuccess;
     const WorkspaceLayout w = workspace_layout(a.num_seqs, a.num_heads, a.head_dim, a.max_blocks);
     if (workspace_bytes < w.total) return cudaErrorInvalidValue;
@@ -697,6 +766,8 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.group = L.group;
     prm.qh = L.qh;
     prm.nhg = L.nhg;
+    prm.active = reinterpret_cast<const int32_t *>(ws + w.active);
+    prm.shared_sms = prefill ? 1 : 0;
     prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim);
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.status = a.status;
@@ -730,27 +801,37 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     }
 
     // plan (and the folded cache write)
-    const size_t plan_smem = sizeof(int32_t) * ((size_t)a.num_seqs + 1) * (write ? 2 : 1);
-    cudaError_t e = cudaFuncSetAttribute(decode_plan_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
+    size_t plan_smem = sizeof(int32_t) * ((size_t)a.num_seqs + 1) * (write ? 2 : 1);
+    if (share_sms && plan_smem < (size_t)kPrefillPlanSmem) plan_smem = kPrefillPlanSmem;
+    auto plan_kern = share_sms ? decode_plan_kernel<true> : decode_plan_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(plan_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (e != cudaSuccess) return e;
     const int64_t max_entries = (int64_t)a.num_seqs * a.max_blocks;
     const int sms = device_sm_count();
+    int grid = sms;
+    if (grid > kPartialCtas) grid = kPartialCtas;
+    DecodeSplit split;
+    split.active = reinterpret_cast<int32_t *>(ws + w.active);
+    split.grid = grid;
+    split.share = share_sms ? 1 : 0;
+    split.causal = a.causal;
+    split.block_ns = (double)kB * a.num_kv_heads * a.head_dim * 2 * 2 / kDecodeBytesPerSmNs;
+    split.pair_ns = 4.0 * a.num_heads * a.head_dim / kPrefillFlopsPerSmNs;
     int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
     if (write && plan_grid < (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32))
         plan_grid = (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32);
     if (plan_grid > 2 * sms) plan_grid = 2 * sms;
     if (plan_grid < 1) plan_grid = 1;
-    e = launch_dependent(decode_plan_kernel, dim3(plan_grid), dim3(kPlanThreads), plan_smem, stream,
+    if (share_sms) ++plan_grid;                 // + the CTA that plans the prefill chunks
+    const PrefillPlanJob pf = share_sms ? *prefill : PrefillPlanJob{};
+    e = launch_dependent(plan_kern, dim3(plan_grid), dim3(kPlanThreads), plan_smem, stream,
                          a.context_lens, a.cu_seqlens_q, a.block_tables, a.num_seqs, a.max_blocks,
                          a.num_blocks, a.total_q, reinterpret_cast<int32_t *>(ws + w.prefix),
-                         reinterpret_cast<StreamEntry *>(ws + w.stream), a.status, job);
+                         reinterpret_cast<StreamEntry *>(ws + w.stream), a.status, job, split, pf);
     if (e != cudaSuccess) return e;
 
-    int grid = sms;
-    if (grid > kPartialCtas) grid = kPartialCtas;
-    return a.head_dim == 64 ? launch_main<64>(a, prm, mk, mv, grid, stream, timed)
-                            : launch_main<128>(a, prm, mk, mv, grid, stream, timed);
+    return a.head_dim == 64 ? launch_main<64>(a, prm, mk, mv, grid, stream, timed, between)
+                            : launch_main<128>(a, prm, mk, mv, grid, stream, timed, between);
 }
 
 }  // namespace pa

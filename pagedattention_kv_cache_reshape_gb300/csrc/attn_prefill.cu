@@ -31,10 +31,9 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
-#include <atomic>
-
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "prefill_plan.cuh"
 
 namespace pa {
 namespace {
@@ -78,121 +77,24 @@ struct PrefillParams {
     float scale_log2;
     int32_t *status;
     int causal;      // 0: encode-only, every row sees the whole sequence
+    // 1: launched behind the decode kernel of the same batch, whose plan launch
+    // also built this kernel's plan.  That plan is complete before the launch
+    // (every decode CTA waited for it before this grid could start), so there is
+    // no wait at the start; the wait for the decode grid comes at the end, so
+    // this grid completes after it and the decode reduce behind it may rely on both.
+    int wait_at_end;
 };
 
-// KV tiles a CTA tile needs: keys up to its last row's position (causal) or
-// the whole sequence; 0 marks a tile the main kernel rejects.
-__device__ __forceinline__ int tile_kv_tiles(int q_len, int ctx, int tile, int cta_shift, int causal) {
-    const int i0 = tile << cta_shift;
-    const int nrows = min(1 << cta_shift, q_len - i0);
-    if (ctx <= 0 || q_len < 2 || q_len > ctx || nrows <= 0) return 0;
-    const int pos_last = causal ? ctx - q_len + i0 + nrows - 1 : ctx - 1;
-    return pos_last / BN + 1;
-}
+static_assert(BN == kPrefillKeysPerTile, "the plan counts KV tiles of the main kernel's width");
 
 // ------------------------------------------------------------------ plan
-// One CTA.  (1) The CTA tiles of every sequence with q_len >= 2, in sequence
-// order, into `scratch`; (2) a counting sort on the number of KV tiles, most
-// first, into `entries`, so the persistent CTAs take the longest work first
-// and finish together; (3) the work counter is reset.
-constexpr int kCostBuckets = 1024;
-constexpr int kPlanSmemTiles = 4096;          // tiles staged in shared memory (else in `scratch`)
-
-__global__ void __launch_bounds__(kPlanThreads)
-    prefill_plan_kernel(const int32_t *__restrict__ cu_seqlens_q, const int32_t *__restrict__ context_lens,
-                        int num_seqs, int cta_shift, int causal, int2 *__restrict__ scratch,
-                        int2 *__restrict__ entries, int32_t *__restrict__ count,
-                        int32_t *__restrict__ next_item, int capacity) {
-    __shared__ int warp_tot[kPlanThreads / 32];
-    __shared__ int bucket[kCostBuckets];
-    __shared__ int2 tiles_s[kPlanSmemTiles];
-    __shared__ uint16_t cost_s[kPlanSmemTiles];
+// One CTA builds the work list (see prefill_plan.cuh).
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PrefillPlanJob job) {
+    extern __shared__ __align__(16) uint8_t plan_smem[];
     // the main kernel may start its prologue now; it waits for this grid
     // before it reads the plan
     grid_dependents_launch();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool in_smem = capacity <= kPlanSmemTiles;
-    int2 *tiles = in_smem ? tiles_s : scratch;
-    const int pos = 1 << cta_shift;
-    for (int b = tid; b < kCostBuckets; b += kPlanThreads) bucket[b] = 0;
-    int running = 0;
-    for (int base = 0; base < num_seqs; base += kPlanThreads) {
-        const int s = base + tid;
-        int nt = 0, q_len = 0, ctx = 0;
-        if (s < num_seqs) {
-            q_len = __ldg(cu_seqlens_q + s + 1) - __ldg(cu_seqlens_q + s);
-            ctx = __ldg(context_lens + s);
-            if (q_len > 1) nt = (q_len + pos - 1) >> cta_shift;
-        }
-        int incl = nt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        int warp_off = 0, chunk_tot = 0;
-        for (int w = 0; w < kPlanThreads / 32; ++w) {
-            if (w < warp) warp_off += warp_tot[w];
-            chunk_tot += warp_tot[w];
-        }
-        // bucket b holds the tiles with kCostBuckets-1-b KV tiles (the last
-        // bucket collects everything longer): ascending buckets = most work first
-        const int first = running + warp_off + incl - nt;
-        for (int t = 0; t < nt; ++t) {
-            if (first + t >= capacity) break;
-            const int c = tile_kv_tiles(q_len, ctx, t, cta_shift, causal);
-            const int b = kCostBuckets - 1 - min(c, kCostBuckets - 1);
-            tiles[first + t] = make_int2(s, t);
-            if (in_smem) cost_s[first + t] = (uint16_t)b;
-            atomicAdd(&bucket[b], 1);
-        }
-        running += chunk_tot;
-        __syncthreads();
-    }
-    const int total = running < capacity ? running : capacity;
-    // exclusive scan of the buckets, kCostBuckets / kPlanThreads per thread
-    constexpr int kPer = kCostBuckets / kPlanThreads;
-    int local[kPer], sum = 0;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        local[k] = bucket[tid * kPer + k];
-        sum += local[k];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int off = incl - sum;
-    for (int w = 0; w < warp; ++w) off += warp_tot[w];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        bucket[tid * kPer + k] = off;
-        off += local[k];
-    }
-    __syncthreads();
-    for (int e = tid; e < total; e += kPlanThreads) {
-        const int2 v = tiles[e];
-        int b;
-        if (in_smem) {
-            b = cost_s[e];
-        } else {
-            const int q0 = __ldg(cu_seqlens_q + v.x);
-            const int c = tile_kv_tiles(__ldg(cu_seqlens_q + v.x + 1) - q0, __ldg(context_lens + v.x), v.y,
-                                        cta_shift, causal);
-            b = kCostBuckets - 1 - min(c, kCostBuckets - 1);
-        }
-        entries[atomicAdd(&bucket[b], 1)] = v;
-    }
-    if (tid == 0) {
-        *count = total;
-        *next_item = 0;
-    }
+    prefill_plan_block(job, plan_smem);
 }
 
 // ------------------------------------------------------------------ main kernel
@@ -231,7 +133,7 @@ __device__ __forceinline__ Item decode_item(const PrefillParams &p, int w) {
     it.i0 = ent.y << cta_shift;
     it.nrows_all = min(1 << cta_shift, it.q_len - it.i0);
     it.pos_base = it.ctx - it.q_len + it.i0;
-    it.nkv = tile_kv_tiles(it.q_len, it.ctx, ent.y, cta_shift, p.causal);
+    it.nkv = prefill_tile_kv_tiles(it.q_len, it.ctx, ent.y, cta_shift, p.causal);
     it.nb = (it.ctx + kB - 1) / kB;
     it.valid = it.nkv > 0 && (int64_t)it.ctx <= (int64_t)p.max_blocks * kB &&
                it.q_len <= p.max_q_len && it.q0 >= 0 && it.q0 + it.q_len <= p.total_q;
@@ -283,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = __shfl_sync(kFull, tid >> 5, 0), lane = tid & 31;
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
         if (tid == 0) set_status(p.status, PA_ERR_CUDA);
+        if (p.wait_at_end) grid_dependency_wait();
         return;
     }
     const int POS = 1 << p.pos_shift;                  // query positions per M-tile
@@ -317,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // everything above overlaps the plan kernel; the plan (and every earlier
     // write in the stream) is visible after this wait
-    grid_dependency_wait();
+    if (!p.wait_at_end) grid_dependency_wait();
     const int total = p.num_entries[0] * p.num_kv_heads;   // plain load: written by the plan grid
     const uint32_t tmem = tmem_base_s;
     // TMEM columns: S_t at t*BN (fp32, BN columns); P_t, bf16 pairs, over the
@@ -342,9 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= TMA producer
         bool ok = true;
         int n = 0, nq = 0;
-        // item `it`: the CTA's own first one, then ids from the counter; decoded
-        // once here and published one item ahead of its use, so no consumer
-        // and no Q copy waits on a fetch at an item boundary
+        // item `it`: the next id from the counter (every item, the first one too:
+        // CTAs that become resident late, behind a concurrent decode kernel,
+        // must not hold on to long items); decoded once here and published one
+        // item ahead of its use, so no consumer and no Q copy waits on a fetch
+        // at an item boundary
         auto publish = [&](int it, Item &I) -> bool {
             bool okp = true;
             int w = total;
@@ -353,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     !mbar_wait(item_empty + it % kItemSlots, (uint32_t)(((it / kItemSlots) - 1) & 1)))
                     okp = false;
                 else
-                    w = it == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.next_item, 1);
+                    w = atomicAdd(p.next_item, 1);
             }
             okp = __shfl_sync(kFull, okp ? 1 : 0, 0) != 0;
             w = __shfl_sync(kFull, w, 0);
@@ -682,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+    if (p.wait_at_end) grid_dependency_wait();
 }
 
 CUresult make_q_map(CUtensorMap *map, const void *q, int total_q, int num_heads, int D, int pos,
@@ -736,18 +642,6 @@ cudaError_t launch_main(const CUtensorMap &mq, const CUtensorMap &mk, const CUte
     return launch_dependent(kern, dim3(grid), dim3(kThreads), smem, stream, mq, mk, mv, prm);
 }
 
-int sm_count() {
-    static std::atomic<int> cache[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    int v = cache[dev].load(std::memory_order_relaxed);
-    if (v == 0) {
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
-        cache[dev].store(v, std::memory_order_relaxed);
-    }
-    return v;
-}
-
 // CTA tiles a batch can produce: at least 2 * 8 positions per tile (G <= 16)
 // plus one partial tile per sequence.
 size_t plan_capacity(int num_seqs, int total_q) { return (size_t)total_q / 8 + num_seqs + 1; }
@@ -768,18 +662,29 @@ size_t prefill_workspace(int num_seqs, int total_q) {
     return align_up(16 + 2 * sizeof(int2) * plan_capacity(num_seqs, total_q), 256);
 }
 
+PrefillPlanJob prefill_plan_job(const AttnArgs &a, void *workspace) {
+    const int G = a.num_heads / a.num_kv_heads;
+    PrefillPlanJob j;
+    j.cu_seqlens_q = a.cu_seqlens_q;
+    j.context_lens = a.context_lens;
+    j.num_seqs = a.num_seqs;
+    j.cta_shift = log2_exact(BM / G) + 1;        // kMT = 2 M-tiles per CTA tile
+    j.causal = a.causal;
+    j.capacity = (int)plan_capacity(a.num_seqs, a.total_q);
+    j.count = static_cast<int32_t *>(workspace);
+    j.next_item = j.count + 1;
+    j.scratch = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + 16);
+    j.entries = j.scratch + j.capacity;
+    return j;
+}
+
 cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool planned) {
     const int G = a.num_heads / a.num_kv_heads;
     const int pos = BM / G;
     const int pos_shift = log2_exact(pos);
-    const int cta_shift = pos_shift + 1;          // kMT = 2 M-tiles of `pos` positions per CTA tile
-    const size_t capacity = plan_capacity(a.num_seqs, a.total_q);
     if (workspace_bytes < prefill_workspace(a.num_seqs, a.total_q)) return cudaErrorInvalidValue;
-    int32_t *count = static_cast<int32_t *>(workspace);
-    int32_t *next_item = count + 1;
-    int2 *scratch = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + 16);
-    int2 *entries = scratch + capacity;
+    const PrefillPlanJob job = prefill_plan_job(a, workspace);
 
     CUtensorMap mq, mk, mv;
     if (make_q_map(&mq, a.q, a.total_q, a.num_heads, a.head_dim, pos, G) != CUDA_SUCCESS ||
@@ -787,19 +692,22 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
         make_kv_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
 
-    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens_q, a.context_lens, a.num_seqs, cta_shift,
-                                                         a.causal, scratch, entries, count, next_item,
-                                                         (int)capacity);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (!planned) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kPrefillPlanSmem);
+        if (e != cudaSuccess) return e;
+        prefill_plan_kernel<<<1, kPlanThreads, kPrefillPlanSmem, stream>>>(job);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
 
     PrefillParams prm;
     prm.cu_seqlens_q = a.cu_seqlens_q;
     prm.context_lens = a.context_lens;
     prm.block_tables = a.block_tables;
-    prm.entries = entries;
-    prm.num_entries = count;
-    prm.next_item = next_item;
+    prm.entries = job.entries;
+    prm.num_entries = job.count;
+    prm.next_item = job.next_item;
     prm.out = static_cast<__nv_bfloat16 *>(a.out);
     prm.num_seqs = a.num_seqs;
     prm.total_q = a.total_q;
@@ -813,9 +721,11 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.status = a.status;
     prm.causal = a.causal;
+    prm.wait_at_end = planned ? 1 : 0;
     // persistent: one CTA per SM, never more CTAs than work items
-    const size_t items = capacity * (size_t)a.num_kv_heads;
-    const int grid = (int)(items < (size_t)sm_count() ? items : (size_t)sm_count());
+    const size_t items = (size_t)job.capacity * (size_t)a.num_kv_heads;
+    const int sms = device_sm_count();
+    const int grid = (int)(items < (size_t)sms ? items : (size_t)sms);
     return a.head_dim == 64 ? launch_main<64>(mq, mk, mv, prm, grid, stream)
                             : launch_main<128>(mq, mk, mv, prm, grid, stream);
 }

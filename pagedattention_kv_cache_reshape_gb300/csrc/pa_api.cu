@@ -29,6 +29,7 @@ int device_sm_count() {
 
 namespace {
 thread_local cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -305,6 +306,21 @@ pa_status varlen_attention(void *out, const void *q, const int32_t *cu_seqlens_q
     // prefill chunks (q_len >= 2) through the tensor-core prefill kernel
     timing_begin(s);
     cudaError_t e = cudaSuccess;
+    if (fast_decode && fast_prefill && max_q_len > 1) {
+        // both parts in one chain on this stream: one plan launch for both,
+        // the decode kernel (it keeps the SMs its share of the work needs and
+        // frees the rest at once), the persistent prefill kernel as its
+        // programmatic dependent (it starts only when every decode CTA is
+        // resident, then takes each SM the decode kernel frees), the reduce
+        uint8_t *pws = static_cast<uint8_t *>(workspace) + dec_ws;
+        const PrefillPlanJob job = prefill_plan_job(a, pws);
+        const std::function<cudaError_t()> prefill = [&]() {
+            return launch_prefill_tc(a, pws, workspace_bytes - dec_ws, s, true);
+        };
+        e = launch_split_decode(a, workspace, dec_ws, s, false, nullptr, &job, &prefill);
+        timing_end(s);
+        return from_cuda(e);
+    }
     if (fast_decode) {
         e = launch_split_decode(a, workspace, dec_ws, s, false);
         if (e != cudaSuccess) return from_cuda(e);

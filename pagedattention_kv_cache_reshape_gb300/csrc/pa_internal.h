@@ -7,9 +7,11 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <functional>
 #include <utility>
 
 #include "pa.h"
+#include "prefill_plan.cuh"
 
 namespace pa {
 
@@ -93,15 +95,26 @@ struct KvWriteArgs {
 // With a.cu_seqlens_q set, only sequences with q_len == 1 are processed and
 // their query/output row is cu_seqlens_q[s].  With `write`, the step's cache
 // write runs in the plan kernel, before any cache read of the decode kernel.
+// With `prefill` (a batch that also has prefill chunks), one extra CTA of the
+// plan launch builds the prefill kernel's work list, the decode kernel keeps
+// only the SMs its share of the work needs, and `between` launches the
+// prefill kernel right behind the decode kernel (before the reduce), so it
+// runs on the SMs the decode kernel leaves.
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                                cudaStream_t stream, bool timed, const KvWriteArgs *write = nullptr);
+                                cudaStream_t stream, bool timed, const KvWriteArgs *write = nullptr,
+                                const PrefillPlanJob *prefill = nullptr,
+                                const std::function<cudaError_t()> *between = nullptr);
 
 // tcgen05 causal prefill for sequences with q_len >= 2 (bf16, head_dim 64/128,
 // q-heads per kv-head a power of two up to 16).
 bool prefill_tc_supported(const AttnArgs &a);
 size_t prefill_workspace(int num_seqs, int total_q);
+// The work list for the prefill kernel in `workspace`.
+PrefillPlanJob prefill_plan_job(const AttnArgs &a, void *workspace);
+// planned: the work list was built by the decode plan launch and this kernel
+// runs behind the decode kernel of the same batch (see launch_split_decode).
 cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspace_bytes,
-                              cudaStream_t stream);
+                              cudaStream_t stream, bool planned = false);
 
 // Launch as a programmatic dependent of the previous kernel in the stream:
 // the kernel calls griddepcontrol.wait before it reads that kernel's output.

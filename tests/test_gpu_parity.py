@@ -223,6 +223,73 @@ def test_run_to_run_determinism():
         assert torch.equal(o, a)
 
 
+def _mixed_for_streams():
+    w = W.mixed(4, oracle_blocks, num_prefill=4, chunk=300, prefix_hi=900, num_decode=60, dec_lo=20,
+                dec_hi=1500, device=DEV)
+    gpu_step(w)                                  # the cache write, then one eager call
+    return w, int(w.q_lens.max())
+
+
+def _varlen(w, out, max_q):
+    return pa.varlen_prefill(w.q, w.cu_seqlens_q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                             w.scale, max_q, out=out)
+
+
+def _capture(w, max_q, warm_up):
+    out = torch.empty_like(w.q)
+    if warm_up:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            _varlen(w, out, max_q)
+        torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _varlen(w, out, max_q)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+    torch.cuda.synchronize()
+    return out
+
+
+def test_mixed_call_in_a_graph_matches_eager_and_oracle():
+    """The decode rows and the prefill chunks of one call run at once (the
+    prefill kernel on the SMs the decode kernel leaves); a CUDA graph of the
+    call gives the eager output bitwise, and it matches the oracle."""
+    w, max_q = _mixed_for_streams()
+    eager = torch.empty_like(w.q)
+    _varlen(w, eager, max_q)
+    torch.cuda.synchronize()
+    assert torch.equal(_capture(w, max_q, warm_up=True), eager)
+    compare(to_f64(eager), oracle_attention(w.to("cpu")), w.dtype, "mixed, parts overlapped")
+
+
+def test_first_call_of_a_thread_captured_matches_eager():
+    """A thread whose very first call is captured into a CUDA graph (no eager
+    warm-up on that thread) gives the eager output bitwise: the call keeps no
+    per-thread state that a capture could not create."""
+    import threading
+    w, max_q = _mixed_for_streams()
+    eager = torch.empty_like(w.q)
+    _varlen(w, eager, max_q)
+    torch.cuda.synchronize()
+    got = {}
+
+    def worker():
+        try:
+            torch.cuda.set_device(0)
+            got["out"] = _capture(w, max_q, warm_up=False)
+        except Exception as ex:  # surfaced below
+            got["error"] = ex
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert "error" not in got, got.get("error")
+    assert torch.equal(got["out"], eager)
+
+
 def test_shared_prefix_identical_outputs():
     """Sequences 0..3 reference the same 256-token prefix blocks read-only and
     hold identical private tails and queries: identical outputs, pool unchanged."""
