@@ -161,6 +161,41 @@ def test_full_size_mixed_sampled():
     compare(got, ref, w.dtype, "mixed_bf16 sampled")
 
 
+def test_prefill_plan_beyond_shared_memory_sampled():
+    """A batch whose prefill work list exceeds what the planner stages in shared
+    memory (more than 4096 CTA tiles of capacity) goes through its global
+    scratch: 72 chunks of 480 rows over prefixes U{0..600} plus 40 decode rows,
+    8 q-heads / 2 kv-heads, sampled rows against the oracle."""
+    rng = np.random.default_rng(11)
+    q_lens = np.concatenate([np.full(72, 480), np.ones(40, dtype=np.int64)])
+    ctx = np.concatenate([480 + rng.integers(0, 601, 72), rng.integers(1, 900, 40)])
+    order = rng.permutation(q_lens.size)
+    w = W.build("big_plan", seed=11, blocks_needed=oracle_blocks, dtype=torch.bfloat16, num_heads=8,
+                num_kv_heads=2, head_dim=128, block_size=16, q_lens=q_lens[order], context_lens=ctx[order],
+                device=DEV)
+    assert w.total_q // 8 + w.num_seqs + 1 > 4096
+    wc = _cpu_copy(w)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _, out = gpu_step(w, dev_status=status)
+    torch.cuda.synchronize()
+    assert pa.get_device_status(status) == 0
+    oracle_write(wc)
+    cu = wc.cu_seqlens_q.numpy()
+    ql = cu[1:] - cu[:-1]
+    rows = []
+    for s_ in range(len(ql)):
+        if ql[s_] == 1:
+            rows.append(cu[s_])
+        else:
+            rows.extend([cu[s_], cu[s_ + 1] - 1, *rng.integers(cu[s_], cu[s_ + 1], 3).tolist()])
+    rows = np.unique(np.array(rows))
+    rr = np.repeat(rows, w.num_heads)
+    hh = np.tile(np.arange(w.num_heads), rows.size)
+    got = to_f64(out)
+    assert np.all(np.isfinite(got))
+    compare(got[rr, hh], oracle_rows(wc, rr, hh), w.dtype, "prefill plan in global scratch")
+
+
 def _poison_unused(w):
     """NaN into every pool slot no sequence reads: unreferenced blocks and the
     tail of each sequence's last block (live slots found with the oracle)."""
