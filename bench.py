@@ -248,9 +248,9 @@ def run_ours(args, world, rank, local):
         pa.varlen_prefill(q, cu, w.k_cache, w.v_cache, bt, ctx, w.scale, max_q, out=o,
                           workspace=workspace, dev_status=status, stream=pa_stream)
 
-    # decode: plan (with the cache write), decode, reduce; mixed: slot mapping,
-    # cache write, plan, decode, reduce, prefill plan, prefill
-    launches_per_step = 3 if decode_only else 7
+    # decode: plan (with the cache write), decode; mixed: slot mapping, cache
+    # write, plan (with the prefill plan), decode, prefill
+    launches_per_step = 2 if decode_only else 5
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()

@@ -21,16 +21,18 @@
 //    Consumer warp kh owns kv-head kh and its G query heads: S = Q K^T and
 //    O += P V run on the tensor cores (mma m16n8k16, bf16 in, fp32 out),
 //    with an online softmax (running max / sum, base-2 exponent) in fp32.
-//    A sequence slice wholly inside one CTA is normalised and stored; a
-//    sequence cut by CTA boundaries leaves (m, l, o) partials.
-//  * reduce kernel -- merges the partials of cut sequences in CTA order:
+//    A sequence slice wholly inside one CTA is normalised and stored.  A
+//    sequence cut by CTA boundaries leaves (m, l, o) partials; the warp that
+//    stores the last of a sequence's pieces (an arrival counter per cut and
+//    kv-head, zeroed by the plan) merges them in CTA order:
 //        M = max m_i, L = sum l_i 2^{m_i - M}, o = sum 2^{m_i - M} o_i / L.
-// The three kernels are launched as programmatic dependents: each is resident
-// early and waits (griddepcontrol.wait) for its predecessor's results only
-// after its prologue, so launch latency overlaps the previous kernel.
+// The two kernels are launched as programmatic dependents: the main kernel is
+// resident early and waits (griddepcontrol.wait) for the plan only after its
+// prologue, so launch latency overlaps the plan.
 // Every cache byte is read once from HBM; the partition depends only on
-// context_lens and the CTA count, so results are bitwise reproducible and do
-// not depend on which physical blocks hold the data.
+// context_lens and the CTA count, and the merge order is fixed, so results
+// are bitwise reproducible and do not depend on which physical blocks hold
+// the data or which CTA finishes first.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -84,6 +86,7 @@ struct DecodeParams {
     int group;     // q-heads per kv-head
     int qh;        // q-heads per CTA = kvh * group
     int nhg;       // kv-head groups
+    int32_t *arrivals;         // [CTAs][KVH] arrival counters of cut sequences, zeroed by the plan
     const int32_t *active;     // CTAs that take a slice (written by the plan; the rest exit)
     int shared_sms;            // 1: `active` is set (a prefill kernel shares the SMs); 0: all CTAs
     int num_stages;
@@ -119,6 +122,8 @@ struct KvWriteJob {
 // per-SM tensor rate, both measured on GB300.
 struct DecodeSplit {
     int32_t *active;
+    int32_t *arrivals;  // zeroed by the plan: [num_arrivals]
+    int num_arrivals;
     int grid;          // CTAs the decode kernel is launched with
     int share;         // 1: a prefill kernel runs beside this one
     int causal;
@@ -149,6 +154,8 @@ __global__ void __launch_bounds__(kPlanThreads)
         prefill_plan_block(prefill, reinterpret_cast<uint8_t *>(pref_s));
         return;
     }
+    if (blockIdx.x == 0)
+        for (int i = tid; i < split.num_arrivals; i += kPlanThreads) split.arrivals[i] = 0;
     if (job.total_new > 0) {
         // ---- the step's cache write: one warp per new token
         int32_t *cu_s = pref_s + num_seqs + 1;
@@ -289,6 +296,77 @@ __device__ __forceinline__ int64_t cta_of(int64_t v, int64_t nv, int64_t p) {
     return ((v + 1) * p - 1) / nv;
 }
 
+// ------------------------------------------------------------------ merge
+// One warp merges the pieces of a cut sequence for nh <= 4 q-heads h0.. of
+// its kv-head group (lane: D/32 consecutive dims of each), in CTA order
+// c0..c1, with the online rule (M, L, acc) <- (max, L a + l b, acc a + o b),
+// a = 2^{M - M'}, b = 2^{m - M'}, per head.  The loads of two pieces of all
+// nh heads are in flight at a time.  The partials were written by other
+// SMs: they are read through L2.
+template <int D>
+__device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t vs, int64_t c0,
+                                             int64_t c1, int64_t NV, int64_t P, int h0, int nh,
+                                             __nv_bfloat16 *dst) {
+    constexpr int kPer = D / 32;
+    constexpr int kH = 4;
+    constexpr int kBatch = 2;
+    const int lane = threadIdx.x & 31;
+    float M[kH], L[kH], acc[kH][kPer];
+#pragma unroll
+    for (int hh = 0; hh < kH; ++hh) {
+        M[hh] = -INFINITY;
+        L[hh] = 0.f;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) acc[hh][u] = 0.f;
+    }
+    for (int64_t cb = c0; cb <= c1; cb += kBatch) {
+        float2 ml[kBatch][kH];
+        float ov[kBatch][kH][kPer];
+        bool use[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int64_t c = cb + k;
+            // CTAs with an empty slice (fewer blocks than CTAs) hold no piece
+            use[k] = c <= c1 && (NV >= P || cta_slice_begin(c, NV, P) < cta_slice_begin(c + 1, NV, P));
+            const int64_t slot = vs + (use[k] ? c : c0);
+#pragma unroll
+            for (int hh = 0; hh < kH; ++hh) {
+                const int h_loc = h0 + (hh < nh ? hh : 0);
+                ml[k][hh] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2));
+                const float *src = p.part_o + (slot * p.qh + h_loc) * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                    ov[k][hh][0] = t.x; ov[k][hh][1] = t.y; ov[k][hh][2] = t.z; ov[k][hh][3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                    ov[k][hh][0] = t.x; ov[k][hh][1] = t.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+            for (int hh = 0; hh < kH; ++hh) {
+                if (!use[k] || ml[k][hh].x == -INFINITY) continue;
+                const float Mn = fmaxf(M[hh], ml[k][hh].x);
+                const float a = fast_exp2(M[hh] - Mn), b = fast_exp2(ml[k][hh].x - Mn);
+                L[hh] = L[hh] * a + ml[k][hh].y * b;
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) acc[hh][u] = acc[hh][u] * a + ov[k][hh][u] * b;
+                M[hh] = Mn;
+            }
+    }
+#pragma unroll
+    for (int hh = 0; hh < kH; ++hh) {
+        if (hh >= nh) break;
+        const float inv = 1.f / L[hh];
+#pragma unroll
+        for (int u = 0; u < kPer; u += 2)
+            *reinterpret_cast<uint32_t *>(dst + hh * D + lane * kPer + u) =
+                pack_bf16x2(acc[hh][u] * inv, acc[hh][u + 1] * inv);
+    }
+}
+
 // ------------------------------------------------------------------ main kernel
 template <int D>
 __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
@@ -322,7 +400,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
     }
     __syncthreads();
     grid_dependency_wait();      // the plan (and everything before it) is complete
-    grid_dependents_launch();    // the reduce kernel may become resident
+    grid_dependents_launch();    // the next kernel may become resident
 
     const int S = p.num_seqs;
     const int64_t T = __ldg(p.prefix + S);
@@ -436,198 +514,167 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
     const int k_tok = ((mi >> 1) << 3) + rr, k_dsub = mi & 1;
     const int v_tok = ((mi & 1) << 3) + rr, v_dsub = mi >> 1;
 
-    float o[kNTiles][4];
-    uint32_t qa[kKSteps][2];
-    float m_run = -INFINITY, l_run = 0.f;
-    int piece_lb0 = 0;
-
-    for (int k = 0; k < nloc; ++k) {
-        const int stage = k % NS;
-        if (*reinterpret_cast<volatile int *>(&abort_flag)) break;
-        if (!mbar_wait(full + stage, (k / NS) & 1)) {
-            if (lane == 0) set_status(p.status, PA_ERR_TIMEOUT);
-            abort_flag = 1;
-            break;
-        }
-        const StageHeader h = hdr[stage];
-        const uint8_t *st = smem + (size_t)stage * stage_bytes;
-        if (h.flags & kFirst) {
-            const uint8_t *qs = st + 2 * kv_tile + (size_t)(kh * G + r) * D * 2;
+    int k = 0;
+    while (k < nloc) {
+        // ---- one piece: the blocks of one sequence (and kv-head group) in this slice;
+        // its accumulators live only here, so the piece's end has registers to spare
+        float o[kNTiles][4];
+        uint32_t qa[kKSteps][2];
+        float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < kKSteps; ++ks) {
-                qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + quad * 2) * 2) : 0u;
-                qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + 8 + quad * 2) * 2) : 0u;
+        for (int j = 0; j < kNTiles; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        StageHeader h;
+        int piece_lb0 = 0;
+        bool aborted = false;
+        for (bool first_block = true;; first_block = false) {
+            const int stage = k % NS;
+            if (*reinterpret_cast<volatile int *>(&abort_flag)) { aborted = true; break; }
+            if (!mbar_wait(full + stage, (k / NS) & 1)) {
+                if (lane == 0) set_status(p.status, PA_ERR_TIMEOUT);
+                abort_flag = 1;
+                aborted = true;
+                break;
             }
+            h = hdr[stage];
+            const uint8_t *st = smem + (size_t)stage * stage_bytes;
+            if (first_block) {
+                const uint8_t *qs = st + 2 * kv_tile + (size_t)(kh * G + r) * D * 2;
 #pragma unroll
-            for (int j = 0; j < kNTiles; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-            m_run = -INFINITY;
-            l_run = 0.f;
-            piece_lb0 = h.lb;
-        }
-        if (h.flags & kValid) {
-            const uint32_t kbase = smem_u32(st + kh * kHeadTileBytes);
-            const uint32_t vbase = smem_u32(st + kv_tile + kh * kHeadTileBytes);
-            // ---- S = Q K^T : two n-tiles of 8 tokens
-            float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int ks = 0; ks < kKSteps; ++ks) {
-                const int chunk = ((ks & 3) << 1) + k_dsub;
-                const uint32_t addr = kbase + (ks >> 2) * (kB * 128) + k_tok * 128 +
-                                      ((chunk ^ (k_tok & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(addr, b0, b1, b2, b3);
-                mma_bf16_16816(sacc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-                mma_bf16_16816(sacc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
-            }
-            // ---- online softmax on row r (tokens 2q, 2q+1, 8+2q, 9+2q)
-            const int ntok = h.ntok;
-            float x[2][2];
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = nt * 8 + quad * 2 + e;
-                    const float val = tok < ntok ? sacc[nt][e] * p.scale_log2 : -INFINITY;
-                    x[nt][e] = val;
-                    tmax = fmaxf(tmax, val);
+                for (int ks = 0; ks < kKSteps; ++ks) {
+                    qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + quad * 2) * 2) : 0u;
+                    qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + 8 + quad * 2) * 2) : 0u;
                 }
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-            const float m_new = fmaxf(m_run, tmax);
-            if (m_new != -INFINITY) {
-                const float alpha = fast_exp2(m_run - m_new);
-                float pr[2][2];
-                float psum = 0.f;
+                piece_lb0 = h.lb;
+            }
+            if (h.flags & kValid) {
+                const uint32_t kbase = smem_u32(st + kh * kHeadTileBytes);
+                const uint32_t vbase = smem_u32(st + kv_tile + kh * kHeadTileBytes);
+                // ---- S = Q K^T : two n-tiles of 8 tokens
+                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < kKSteps; ++ks) {
+                    const int chunk = ((ks & 3) << 1) + k_dsub;
+                    const uint32_t addr = kbase + (ks >> 2) * (kB * 128) + k_tok * 128 +
+                                          ((chunk ^ (k_tok & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(addr, b0, b1, b2, b3);
+                    mma_bf16_16816(sacc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+                    mma_bf16_16816(sacc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+                }
+                // ---- online softmax on row r (tokens 2q, 2q+1, 8+2q, 9+2q)
+                const int ntok = h.ntok;
+                float x[2][2];
+                float tmax = -INFINITY;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        pr[nt][e] = fast_exp2(x[nt][e] - m_new);
-                        psum += pr[nt][e];
+                        const int tok = nt * 8 + quad * 2 + e;
+                        const float val = tok < ntok ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+                        x[nt][e] = val;
+                        tmax = fmaxf(tmax, val);
                     }
-                l_run = l_run * alpha + psum;
-                m_run = m_new;
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+                const float m_new = fmaxf(m_run, tmax);
+                if (m_new != -INFINITY) {
+                    const float alpha = fast_exp2(m_run - m_new);
+                    float pr[2][2];
+                    float psum = 0.f;
 #pragma unroll
-                for (int j = 0; j < kNTiles; ++j) {
-                    o[j][0] *= alpha;
-                    o[j][1] *= alpha;
-                }
-                const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
-                const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
-                // masks for value rows past the sequence end (they may hold anything)
-                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                if (ntok < kB) {
-                    const int t0 = quad * 2;
-                    mlo = (t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u);
-                    mhi = (t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u);
-                }
-                // ---- O += P V : D/8 n-tiles of 8 dims, k = 16 tokens
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int j2 = 0; j2 < kNTiles / 2; ++j2) {
-                    const int chunk = ((j2 & 3) << 1) + v_dsub;
-                    const uint32_t addr = vbase + (j2 >> 2) * (kB * 128) + v_tok * 128 +
-                                          ((chunk ^ (v_tok & 7)) << 4);
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_t(addr, v0, v1, v2, v3);
-                    v0 &= mlo; v2 &= mlo; v1 &= mhi; v3 &= mhi;
-                    mma_bf16_16816(o[2 * j2], pa0, 0u, pa2, 0u, v0, v1);
-                    mma_bf16_16816(o[2 * j2 + 1], pa0, 0u, pa2, 0u, v2, v3);
+                        for (int e = 0; e < 2; ++e) {
+                            pr[nt][e] = fast_exp2(x[nt][e] - m_new);
+                            psum += pr[nt][e];
+                        }
+                    l_run = l_run * alpha + psum;
+                    m_run = m_new;
+#pragma unroll
+                    for (int j = 0; j < kNTiles; ++j) {
+                        o[j][0] *= alpha;
+                        o[j][1] *= alpha;
+                    }
+                    const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
+                    const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
+                    // masks for value rows past the sequence end (they may hold anything)
+                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                    if (ntok < kB) {
+                        const int t0 = quad * 2;
+                        mlo = (t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u);
+                        mhi = (t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u);
+                    }
+                    // ---- O += P V : D/8 n-tiles of 8 dims, k = 16 tokens
+#pragma unroll
+                    for (int j2 = 0; j2 < kNTiles / 2; ++j2) {
+                        const int chunk = ((j2 & 3) << 1) + v_dsub;
+                        const uint32_t addr = vbase + (j2 >> 2) * (kB * 128) + v_tok * 128 +
+                                              ((chunk ^ (v_tok & 7)) << 4);
+                        uint32_t v0, v1, v2, v3;
+                        ldsm_x4_t(addr, v0, v1, v2, v3);
+                        v0 &= mlo; v2 &= mlo; v1 &= mhi; v3 &= mhi;
+                        mma_bf16_16816(o[2 * j2], pa0, 0u, pa2, 0u, v0, v1);
+                        mma_bf16_16816(o[2 * j2 + 1], pa0, 0u, pa2, 0u, v2, v3);
+                    }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + stage);
+            ++k;
+            if ((h.flags & kLast) || k >= nloc) break;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty + stage);
+        if (aborted) break;
 
-        if (h.flags & kLast) {
-            float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
-            l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-            const bool whole = piece_lb0 == 0 && (h.flags & kSeqEnd);
-            const int h_loc = kh * G + r;
+        // ---- the piece's end
+        float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+        const bool whole = piece_lb0 == 0 && (h.flags & kSeqEnd);
+        const int h_loc = kh * G + r;
+        const int64_t out_row = (int64_t)h.qrow * p.num_heads + (int64_t)h.hg * p.qh;
+        if (whole) {
             if (row_ok) {
-                if (whole) {
-                    const float inv = 1.f / l_row;
-                    __nv_bfloat16 *dst = p.out + ((int64_t)h.qrow * p.num_heads +
-                                                  (int64_t)h.hg * p.qh + h_loc) * D + quad * 2;
+                const float inv = 1.f / l_row;
+                __nv_bfloat16 *dst = p.out + (out_row + h_loc) * D + quad * 2;
 #pragma unroll
-                    for (int j = 0; j < kNTiles; ++j)
-                        *reinterpret_cast<uint32_t *>(dst + j * 8) =
-                            pack_bf16x2(o[j][0] * inv, o[j][1] * inv);
-                } else {
-                    const int64_t slot = (int64_t)h.hg * S + h.seq + blockIdx.x;
-                    float *dst = p.part_o + (slot * p.qh + h_loc) * D + quad * 2;
-#pragma unroll
-                    for (int j = 0; j < kNTiles; ++j)
-                        *reinterpret_cast<float2 *>(dst + j * 8) = make_float2(o[j][0], o[j][1]);
-                    if (quad == 0)
-                        *reinterpret_cast<float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2) =
-                            make_float2(m_run, l_row);
-                }
+                for (int j = 0; j < kNTiles; ++j)
+                    *reinterpret_cast<uint32_t *>(dst + j * 8) = pack_bf16x2(o[j][0] * inv, o[j][1] * inv);
             }
+            continue;
+        }
+        // a piece of a sequence cut by CTA boundaries: store it, count it in;
+        // the warp that stores the last of the sequence's pieces merges them
+        const int64_t vs = (int64_t)h.hg * S + h.seq;
+        const int64_t slot = vs + blockIdx.x;
+        if (row_ok) {
+            float *dst = p.part_o + (slot * p.qh + h_loc) * D + quad * 2;
+#pragma unroll
+            for (int j = 0; j < kNTiles; ++j)
+                *reinterpret_cast<float2 *>(dst + j * 8) = make_float2(o[j][0], o[j][1]);
+            if (quad == 0)
+                *reinterpret_cast<float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2) = make_float2(m_run, l_row);
+        }
+        // (the stream's sizes are reloaded here rather than kept in registers through the loop)
+        const int64_t Tt = __ldg(p.prefix + S);
+        const int64_t NVt = Tt * p.nhg;
+        const int64_t Pt = p.shared_sms ? min((int64_t)gridDim.x, (int64_t)__ldg(p.active)) : (int64_t)gridDim.x;
+        const int64_t b0 = __ldg(p.prefix + h.seq), b1 = __ldg(p.prefix + h.seq + 1);
+        const int64_t c0 = cta_of(h.hg * Tt + b0, NVt, Pt), c1 = cta_of(h.hg * Tt + b1 - 1, NVt, Pt);
+        int pieces = (int)(c1 - c0 + 1);
+        if (NVt < Pt) {
+            pieces = 0;
+            for (int64_t c = c0; c <= c1; ++c)
+                pieces += cta_slice_begin(c, NVt, Pt) < cta_slice_begin(c + 1, NVt, Pt) ? 1 : 0;
+        }
+        __syncwarp();   // every lane's stores precede lane 0's release
+        int merge = 0;
+        if (lane == 0) merge = atomic_add_acq_rel_gpu(p.arrivals + c0 * kvh + kh, 1) == pieces - 1;
+        merge = __shfl_sync(0xffffffffu, merge, 0);   // (also orders lane 0's acquire before the loads)
+        if (merge) {
+            for (int g = 0; g < G; g += 4)
+                merge_pieces<D>(p, vs, c0, c1, NVt, Pt, kh * G + g, G - g < 4 ? G - g : 4,
+                                p.out + (out_row + kh * G + g) * D);
         }
     }
-}
-
-// ------------------------------------------------------------------ reduce
-// One warp per (virtual sequence, q-head) of a cut sequence.  Pieces are
-// combined in CTA order with the online rule (M, L, acc) <- (max, L a + l b,
-// acc a + o b), a = 2^{M - M'}, b = 2^{m - M'}; four pieces' loads are in
-// flight at a time.
-template <int D>
-__global__ void __launch_bounds__(256)
-    split_decode_reduce_kernel(const DecodeParams p, int num_ctas) {
-    grid_dependency_wait();  // the decode kernel's partials are complete
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const int S = p.num_seqs;
-    const int vs = gw / p.qh, h_loc = gw % p.qh;
-    if (vs >= p.nhg * S) return;
-    const int hg = vs / S, s = vs % S;
-    const int64_t T = __ldg(p.prefix + S);
-    const int64_t NV = T * p.nhg;
-    const int64_t P = p.shared_sms ? min((int64_t)num_ctas, (int64_t)__ldg(p.active)) : (int64_t)num_ctas;
-    const int64_t b0 = __ldg(p.prefix + s), b1 = __ldg(p.prefix + s + 1);
-    if (b1 == b0) return;
-    const int64_t c0 = cta_of(hg * T + b0, NV, P);
-    const int64_t c1 = cta_of(hg * T + b1 - 1, NV, P);
-    if (c0 == c1) return;  // whole sequence inside one CTA: already written
-    constexpr int kPer = D / 32;
-    constexpr int kBatch = 4;
-    float M = -INFINITY, L = 0.f, acc[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) acc[u] = 0.f;
-    for (int64_t cb = c0; cb <= c1; cb += kBatch) {
-        float2 ml[kBatch];
-        float ov[kBatch][kPer];
-        bool use[kBatch];
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int64_t c = cb + k;
-            // CTAs with an empty slice (fewer blocks than CTAs) wrote nothing
-            use[k] = c <= c1 && (NV >= P || cta_slice_begin(c, NV, P) < cta_slice_begin(c + 1, NV, P));
-            const int64_t slot = vs + (use[k] ? c : c0);
-            ml[k] = *reinterpret_cast<const float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2);
-            const float *src = p.part_o + (slot * p.qh + h_loc) * D + lane * kPer;
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) ov[k][u] = src[u];
-        }
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            if (!use[k] || ml[k].x == -INFINITY) continue;
-            const float Mn = fmaxf(M, ml[k].x);
-            const float a = fast_exp2(M - Mn), b = fast_exp2(ml[k].x - Mn);
-            L = L * a + ml[k].y * b;
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) acc[u] = acc[u] * a + ov[k][u] * b;
-            M = Mn;
-        }
-    }
-    const int qrow = __ldg(&p.stream[b0].qrow);
-    __nv_bfloat16 *dst = p.out + ((int64_t)qrow * p.num_heads + (int64_t)hg * p.qh + h_loc) * D + lane * kPer;
-    const float inv = 1.f / L;
-#pragma unroll
-    for (int u = 0; u < kPer; u += 2)
-        *reinterpret_cast<uint32_t *>(dst + u) = pack_bf16x2(acc[u] * inv, acc[u + 1] * inv);
 }
 
 // ------------------------------------------------------------------ host side
@@ -676,8 +723,12 @@ Layout decode_layout(int num_heads, int num_kv_heads) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace: the plan's prefix [S + 1] and SM split, the arrival counters of
+// cut sequences [kPartialCtas][kMaxKvhPerCta], the block stream [S * max_blocks],
+// then the partials, slot = hg*S + s + CTA (< NHG*S + CTAs): (m, l)
+// [slots][QH][2] and o [slots][QH][D], fp32.
 struct WorkspaceLayout {
-    size_t prefix, active, stream, part_ml, part_o, total;
+    size_t prefix, active, arrivals, stream, part_ml, part_o, total;
 };
 
 WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_blocks) {
@@ -685,7 +736,8 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
     const size_t slots_heads = ((size_t)num_seqs + kPartialCtas) * num_heads;
     w.prefix = 0;
     w.active = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 16);
-    w.stream = align_up(w.active + sizeof(int32_t), 256);
+    w.arrivals = align_up(w.active + sizeof(int32_t), 256);
+    w.stream = align_up(w.arrivals + sizeof(int32_t) * kPartialCtas * kMaxKvhPerCta, 256);
     w.part_ml = align_up(w.stream + sizeof(StreamEntry) * (size_t)num_seqs * max_blocks, 256);
     w.part_o = align_up(w.part_ml + sizeof(float) * 2 * slots_heads, 256);
     w.total = align_up(w.part_o + sizeof(float) * (size_t)head_dim * slots_heads, 256);
@@ -693,9 +745,8 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
 }
 
 template <int D>
-cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtensorMap &mk,
-                        const CUtensorMap &mv, int grid, cudaStream_t stream, bool timed,
-                        const std::function<cudaError_t()> *between) {
+cudaError_t launch_main(const DecodeParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
+                        int grid, cudaStream_t stream, bool timed) {
     const int kv_tile = prm.kvh * kB * D * 2;
     const int stage_bytes = (int)align_up(2 * kv_tile + prm.qh * D * 2, 1024);
     const size_t smem = 1024 + (size_t)prm.num_stages * (stage_bytes + sizeof(StageHeader) + 16);
@@ -705,14 +756,7 @@ cudaError_t launch_main(const AttnArgs &a, const DecodeParams &prm, const CUtens
     if (timed) timing_begin(stream);
     e = launch_dependent(kern, dim3(grid), dim3(32 * (prm.kvh + 1)), smem, stream, mk, mv, prm);
     if (timed) timing_end(stream);
-    if (e != cudaSuccess) return e;
-    if (between) {
-        e = (*between)();
-        if (e != cudaSuccess) return e;
-    }
-    const int warps = prm.nhg * prm.num_seqs * prm.qh;
-    return launch_dependent(split_decode_reduce_kernel<D>, dim3((warps + 7) / 8), dim3(256), 0, stream,
-                            prm, grid);
+    return e;
 }
 
 int stages_for(int kvh, int qh, int D) {
@@ -767,6 +811,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.qh = L.qh;
     prm.nhg = L.nhg;
     prm.active = reinterpret_cast<const int32_t *>(ws + w.active);
+    prm.arrivals = reinterpret_cast<int32_t *>(ws + w.arrivals);
     prm.shared_sms = prefill ? 1 : 0;
     prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim);
     prm.scale_log2 = a.scale * 1.4426950408889634f;
@@ -812,6 +857,8 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     if (grid > kPartialCtas) grid = kPartialCtas;
     DecodeSplit split;
     split.active = reinterpret_cast<int32_t *>(ws + w.active);
+    split.arrivals = prm.arrivals;
+    split.num_arrivals = grid * L.kvh;
     split.grid = grid;
     split.share = share_sms ? 1 : 0;
     split.causal = a.causal;
@@ -830,8 +877,10 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
                          reinterpret_cast<StreamEntry *>(ws + w.stream), a.status, job, split, pf);
     if (e != cudaSuccess) return e;
 
-    return a.head_dim == 64 ? launch_main<64>(a, prm, mk, mv, grid, stream, timed, between)
-                            : launch_main<128>(a, prm, mk, mv, grid, stream, timed, between);
+    e = a.head_dim == 64 ? launch_main<64>(prm, mk, mv, grid, stream, timed)
+                         : launch_main<128>(prm, mk, mv, grid, stream, timed);
+    if (e != cudaSuccess) return e;
+    return between ? (*between)() : cudaSuccess;
 }
 
 }  // namespace pa

@@ -81,7 +81,7 @@ struct PrefillParams {
     // also built this kernel's plan.  That plan is complete before the launch
     // (every decode CTA waited for it before this grid could start), so there is
     // no wait at the start; the wait for the decode grid comes at the end, so
-    // this grid completes after it and the decode reduce behind it may rely on both.
+    // this grid completes after it and later work may rely on both.
     int wait_at_end;
 };
 

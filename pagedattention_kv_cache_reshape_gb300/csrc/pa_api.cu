@@ -311,7 +311,7 @@ pa_status varlen_attention(void *out, const void *q, const int32_t *cu_seqlens_q
         // the decode kernel (it keeps the SMs its share of the work needs and
         // frees the rest at once), the persistent prefill kernel as its
         // programmatic dependent (it starts only when every decode CTA is
-        // resident, then takes each SM the decode kernel frees), the reduce
+        // resident, then takes each SM the decode kernel frees)
         uint8_t *pws = static_cast<uint8_t *>(workspace) + dec_ws;
         const PrefillPlanJob job = prefill_plan_job(a, pws);
         const std::function<cudaError_t()> prefill = [&]() {

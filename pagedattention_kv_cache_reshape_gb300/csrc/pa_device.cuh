@@ -37,6 +37,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// atomicAdd with acquire-release semantics at GPU scope: the caller's earlier
+// writes (and those ordered before it by a warp or CTA barrier) are visible
+// to whoever reads the new value, and the caller sees what was published
+// before the values it read.  Returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // max of three (NaN operands are ignored, as for fmaxf)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;

@@ -98,8 +98,8 @@ struct KvWriteArgs {
 // With `prefill` (a batch that also has prefill chunks), one extra CTA of the
 // plan launch builds the prefill kernel's work list, the decode kernel keeps
 // only the SMs its share of the work needs, and `between` launches the
-// prefill kernel right behind the decode kernel (before the reduce), so it
-// runs on the SMs the decode kernel leaves.
+// prefill kernel right behind the decode kernel, so it runs on the SMs the
+// decode kernel leaves.
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
                                 cudaStream_t stream, bool timed, const KvWriteArgs *write = nullptr,
                                 const PrefillPlanJob *prefill = nullptr,
