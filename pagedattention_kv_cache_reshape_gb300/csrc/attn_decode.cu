@@ -112,6 +112,7 @@ struct KvWriteJob {
     int64_t *slot_mapping;
     int row_vecs;            // 16-byte vectors per token row
     int64_t pool_slots;
+    int first_cta;           // the plan launch's CTAs from here on do the write
 };
 
 // How many of the decode kernel's CTAs take a slice.  Alone on the GPU,
@@ -132,8 +133,11 @@ struct DecodeSplit {
 };
 
 // ------------------------------------------------------------------ plan
-// kShare: the batch also has prefill chunks (the extra CTA plans them and CTA
-// 0 sets the SM split); decode-only calls run the plain instantiation.
+// CTAs [0, job.first_cta) build the block stream (CTA 0 also zeroes the
+// arrival counters); the CTAs after them, up to the last, write the step's
+// new tokens into the cache, concurrently.  kShare: the batch also has
+// prefill chunks (the last CTA plans them and CTA 0 sets the SM split);
+// decode-only calls run the plain instantiation.
 template <bool kShare>
 __global__ void __launch_bounds__(kPlanThreads)
     decode_plan_kernel(const int32_t *__restrict__ context_lens,
@@ -142,40 +146,65 @@ __global__ void __launch_bounds__(kPlanThreads)
                        int num_blocks, int total_q, int32_t *__restrict__ prefix,
                        StreamEntry *__restrict__ stream, int32_t *status, const KvWriteJob job,
                        const DecodeSplit split, const PrefillPlanJob prefill) {
-    extern __shared__ __align__(16) int32_t pref_s[];  // [num_seqs + 1], then cu_new [num_seqs + 1]
+    extern __shared__ __align__(16) int32_t pref_s[];  // [num_seqs + 1]
     __shared__ int32_t warp_tot[kPlanThreads / 32];
     __shared__ double pair_tot[kPlanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();      // inputs may come from the previous kernel
     grid_dependents_launch();    // the decode kernel may start its prologue
     // with prefill chunks in the batch, the last CTA builds their work list
-    const int dgrid = (int)gridDim.x - (kShare ? 1 : 0);   // CTAs of the decode plan proper
+    const int dgrid = (int)gridDim.x - (kShare ? 1 : 0);   // CTAs of the plan and the cache write
     if (kShare && (int)blockIdx.x == dgrid) {
         prefill_plan_block(prefill, reinterpret_cast<uint8_t *>(pref_s));
         return;
     }
     if (blockIdx.x == 0)
         for (int i = tid; i < split.num_arrivals; i += kPlanThreads) split.arrivals[i] = 0;
-    if (job.total_new > 0) {
-        // ---- the step's cache write: one warp per new token
-        int32_t *cu_s = pref_s + num_seqs + 1;
-        for (int i = tid; i <= num_seqs; i += kPlanThreads) cu_s[i] = __ldg(job.cu_new + i);
-        __syncthreads();
+    if ((int)blockIdx.x >= job.first_cta) {
+        // ---- the step's cache write, beside the plan: one warp per new token
         const int warps = kPlanThreads / 32;
-        for (int t = blockIdx.x * warps + warp; t < job.total_new; t += dgrid * warps) {
+        const int wctas = dgrid - job.first_cta;
+        constexpr int kPre = 4;   // 16-byte vectors per lane loaded before the slot is known
+        for (int t = ((int)blockIdx.x - job.first_cta) * warps + warp; t < job.total_new; t += wctas * warps) {
+            const uint4 *ks = job.key + t * job.key_stride_v;
+            const uint4 *vs = job.value + t * job.value_stride_v;
+            // the rows depend only on t: their loads overlap the slot's dependent loads
+            uint4 kr[kPre], vr[kPre];
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) {
+                const int i = lane + 32 * u;
+                if (i < job.row_vecs) {
+                    kr[u] = __ldg(ks + i);
+                    vr[u] = __ldg(vs + i);
+                }
+            }
             int64_t slot = -1;
             if (lane == 0) {
-                int lo = 0, hi = num_seqs;  // last s with cu_new[s] <= t
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (cu_s[mid] <= t) lo = mid; else hi = mid;
+                // the token's sequence: s = t when sequence t has exactly its one new
+                // token at t (checked), else the last s with cu_new[s] <= t
+                int s = -1, c0 = 0, st = 0;
+                if (t < num_seqs) {
+                    c0 = __ldg(job.cu_new + t);
+                    const int c1 = __ldg(job.cu_new + t + 1);
+                    st = __ldg(job.seq_start + t);
+                    if (c0 <= t && t < c1) s = t;
                 }
-                const int64_t pos = (int64_t)__ldg(job.seq_start + lo) + (t - cu_s[lo]);
+                if (s < 0) {
+                    int lo = 0, hi = num_seqs;
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (__ldg(job.cu_new + mid) <= t) lo = mid; else hi = mid;
+                    }
+                    s = lo;
+                    c0 = __ldg(job.cu_new + lo);
+                    st = __ldg(job.seq_start + lo);
+                }
+                const int64_t pos = (int64_t)st + (t - c0);
                 const int64_t logical = pos / kB;
                 if (pos < 0 || logical >= max_blocks) {
                     set_status(status, PA_ERR_OUT_OF_RANGE);
                 } else {
-                    const int32_t phys = __ldg(block_tables + (int64_t)lo * max_blocks + logical);
+                    const int32_t phys = __ldg(block_tables + (int64_t)s * max_blocks + logical);
                     if (phys < 0 || phys >= num_blocks) set_status(status, PA_ERR_OUT_OF_RANGE);
                     else slot = (int64_t)phys * kB + (pos - logical * kB);
                 }
@@ -183,19 +212,26 @@ __global__ void __launch_bounds__(kPlanThreads)
             }
             slot = __shfl_sync(0xffffffffu, slot, 0);
             if (slot < 0 || slot >= job.pool_slots) continue;
-            const uint4 *ks = job.key + t * job.key_stride_v;
-            const uint4 *vs = job.value + t * job.value_stride_v;
             uint4 *kd = job.k_cache + slot * job.row_vecs;
             uint4 *vd = job.v_cache + slot * job.row_vecs;
-            for (int i = lane; i < job.row_vecs; i += 32) {
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) {
+                const int i = lane + 32 * u;
+                if (i < job.row_vecs) {
+                    kd[i] = kr[u];
+                    vd[i] = vr[u];
+                }
+            }
+            for (int i = lane + 32 * kPre; i < job.row_vecs; i += 32) {
                 const uint4 kv = __ldg(ks + i);
                 const uint4 vv = __ldg(vs + i);
                 kd[i] = kv;
                 vd[i] = vv;
             }
         }
-        __syncthreads();
+        return;
     }
+    const int pgrid = job.first_cta;   // CTAs of the plan proper
     int running = 0;
     double pairs = 0.0;   // causal (query, key) pairs of this thread's prefill rows
     for (int base = 0; base < num_seqs; base += kPlanThreads) {
@@ -263,7 +299,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     const int T = running;
     if (blockIdx.x == 0)
         for (int s = tid; s <= num_seqs; s += kPlanThreads) prefix[s] = pref_s[s];
-    for (int b = blockIdx.x * kPlanThreads + tid; b < T; b += dgrid * kPlanThreads) {
+    for (int b = blockIdx.x * kPlanThreads + tid; b < T; b += pgrid * kPlanThreads) {
         int lo = 0, hi = num_seqs;  // last s with pref_s[s] <= b
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -846,7 +882,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     }
 
     // plan (and the folded cache write)
-    size_t plan_smem = sizeof(int32_t) * ((size_t)a.num_seqs + 1) * (write ? 2 : 1);
+    size_t plan_smem = sizeof(int32_t) * ((size_t)a.num_seqs + 1);
     if (share_sms && plan_smem < (size_t)kPrefillPlanSmem) plan_smem = kPrefillPlanSmem;
     auto plan_kern = share_sms ? decode_plan_kernel<true> : decode_plan_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(plan_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
@@ -865,10 +901,12 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     split.block_ns = (double)kB * a.num_kv_heads * a.head_dim * 2 * 2 / kDecodeBytesPerSmNs;
     split.pair_ns = 4.0 * a.num_heads * a.head_dim / kPrefillFlopsPerSmNs;
     int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
-    if (write && plan_grid < (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32))
-        plan_grid = (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32);
     if (plan_grid > 2 * sms) plan_grid = 2 * sms;
     if (plan_grid < 1) plan_grid = 1;
+    int write_grid = write ? (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32) : 0;
+    if (write_grid > 2 * sms) write_grid = 2 * sms;
+    job.first_cta = plan_grid;
+    plan_grid += write_grid;                    // + the CTAs of the cache write
     if (share_sms) ++plan_grid;                 // + the CTA that plans the prefill chunks
     const PrefillPlanJob pf = share_sms ? *prefill : PrefillPlanJob{};
     e = launch_dependent(plan_kern, dim3(plan_grid), dim3(kPlanThreads), plan_smem, stream,
