@@ -352,23 +352,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dq = umma_desc_sw128(q_addr, 16, 1024);
         const uint64_t dk = umma_desc_sw128(kv_addr, 16, 1024);
         const uint64_t dv = umma_desc_sw128(kv_addr, kPlaneKV, 1024);
+        // The K loops go out four MMAs per asm block (one 64-wide plane of the
+        // swizzled operands each): fewer instructions between MMAs lets the
+        // single issuing thread keep closer to the tensor pipe.
         auto issue_qk = [&](int t, int nk) {      // S_t = Q_t K^T, K in ring entry nk
             const uint32_t ko = (uint32_t)slot_of(nk) * kSlotBytes;
+            if (leader) {
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * kPlaneKV + (ks & 3) * 32;
-                const uint32_t offq = t * kQBytes + (ks >> 2) * kPlaneQ + (ks & 3) * 32;
-                if (leader)
-                    umma_bf16(tmem + s_col(t), dq + (offq >> 4), dk + ((ko + off) >> 4), kIdescQK, ks > 0);
+                for (int pl = 0; pl < D / 64; ++pl)
+                    umma_bf16_k64(tmem + s_col(t), dq + ((uint32_t)(t * kQBytes + pl * kPlaneQ) >> 4),
+                                  dk + ((ko + pl * kPlaneKV) >> 4), kIdescQK, pl > 0 ? 1u : 0u);
             }
+            __syncwarp();
         };
         auto issue_pv = [&](int t, int nv, bool first) {   // O_t (+)= P_t V, V in ring entry nv
             const uint32_t vo = (uint32_t)slot_of(nv) * kSlotBytes;
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                if (leader)
-                    umma_bf16_tmem_a(tmem + o_col(t), tmem + s_col(t) + kk * 8, dv + ((vo + kk * 2048) >> 4),
-                                     kIdescPV, (!first || kk > 0) ? 1u : 0u);
+                for (int kq = 0; kq < BN / 64; ++kq)   // 64 keys (4 MMAs of 16) per block
+                    umma_bf16_tmem_a_k64(tmem + o_col(t), tmem + s_col(t) + kq * 32,
+                                         dv + ((vo + kq * 4 * 2048) >> 4), kIdescPV, 2048 >> 4,
+                                         (!first || kq > 0) ? 1u : 0u);
+            }
+            __syncwarp();
         };
         auto commit = [&](uint64_t *bar) {
             if (leader) umma_commit(bar);

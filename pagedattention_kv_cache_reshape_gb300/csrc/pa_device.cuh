@@ -215,6 +215,43 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// Four chained MMAs over K = 64 (one 128-byte swizzled plane of both
+// operands): step k reads A and B 32 bytes further along their rows (the
+// descriptors' address field, in 16-byte units, advances by 2).  The first
+// accumulates into D only if `accumulate`; the rest always do.  One asm block
+// keeps the issuing thread's instruction stream to the MMAs and two adds each.
+__device__ __forceinline__ void umma_bf16_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .b64 a, b;\n\t.reg .pred p0, p1;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(1u));
+}
+
+// Four chained MMAs with A from tensor memory over K = 64: step k reads A 8
+// columns (16 bf16 K values) further and B `b_step` (16-byte units) further.
+__device__ __forceinline__ void umma_bf16_tmem_a_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t b_step, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .b64 b, bs;\n\t.reg .b32 a;\n\t.reg .pred p0, p1;\n\t"
+        "setp.ne.b32 p0, %5, 0;\n\tsetp.ne.b32 p1, %6, 0;\n\tcvt.u64.u32 bs, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "add.s32 a, %1, 8;\n\tadd.s64 b, %2, bs;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.s32 a, a, 8;\n\tadd.s64 b, b, bs;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.s32 a, a, 8;\n\tadd.s64 b, b, bs;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(b_step), "r"(accumulate), "r"(1u));
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
