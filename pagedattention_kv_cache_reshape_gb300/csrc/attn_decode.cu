@@ -18,9 +18,11 @@
 //    KVH kv-heads (32 KB of K and 32 KB of V for 8 heads x 128 dims) with one
 //    TMA tensor copy each into a ring of shared-memory stages (128-byte
 //    swizzle), plus the sequence's query heads when a new sequence starts.
-//    Consumer warp kh owns kv-head kh and its G query heads: S = Q K^T and
-//    O += P V run on the tensor cores (mma m16n8k16, bf16 in, fp32 out),
-//    with an online softmax (running max / sum, base-2 exponent) in fp32.
+//    A consumer warp owns up to 8 q-heads of one kv-head (a kv-head with G > 8
+//    q-heads gets ceil(G/8) warps): S^T = K Q^T and O^T += V^T P^T run on the
+//    tensor cores (mma m16n8k16, bf16 in, fp32 out), the block's 16 tokens in
+//    M and the q-heads in N, with an online softmax (running max / sum,
+//    base-2 exponent) in fp32.
 //    A sequence slice wholly inside one CTA is normalised and stored.  A
 //    sequence cut by CTA boundaries leaves (m, l, o) partials; the warp that
 //    stores the last of a sequence's pieces (an arrival counter per cut and
@@ -48,8 +50,10 @@ namespace {
 
 constexpr int kB = kBlockSize;  // 16 tokens per block
 constexpr int kMaxKvhPerCta = 8;
+constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxQHeadsPerCta = 32;
-constexpr int kMaxGroup = 16;       // one m16 tile of query heads per kv-head
+constexpr int kHeadsPerWarp = 8;    // the N of one m16n8k16 product: q-heads per consumer warp
+constexpr int kMaxGroup = 32;       // q-heads per kv-head
 constexpr int kMaxSeqs = 16384;     // prefix of all sequences kept in shared memory
 constexpr int kPartialCtas = 512;   // partial slots reserved for CTA boundaries
 constexpr int kPlanThreads = 256;
@@ -83,10 +87,12 @@ struct DecodeParams {
     int num_seqs;
     int num_heads;
     int kvh;       // kv-heads per CTA
+    int wpk;       // consumer warps per kv-head: ceil(group / 8)
+    int gw;        // q-heads per consumer warp: ceil(group / wpk)
     int group;     // q-heads per kv-head
     int qh;        // q-heads per CTA = kvh * group
     int nhg;       // kv-head groups
-    int32_t *arrivals;         // [CTAs][KVH] arrival counters of cut sequences, zeroed by the plan
+    int32_t *arrivals;         // [CTAs][consumer warps] arrival counters of cut sequences, zeroed by the plan
     const int32_t *active;     // CTAs that take a slice (written by the plan; the rest exit)
     int shared_sms;            // 1: `active` is set (a prefill kernel shares the SMs); 0: all CTAs
     int num_stages;
@@ -405,17 +411,17 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t vs, 
 
 // ------------------------------------------------------------------ main kernel
 template <int D>
-__global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
+__global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     split_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
     constexpr int kHeadTileBytes = kB * D * 2;    // one kv-head of one block
     constexpr int kKSteps = D / 16;
-    constexpr int kNTiles = D / 8;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     const int kvh = p.kvh, NS = p.num_stages;
+    const int cwarps = kvh * p.wpk;   // consumer warps; the producer is the next one
     const int kv_tile = kvh * kHeadTileBytes;
     const int q_tile = p.qh * D * 2;
     const int stage_bytes = (2 * kv_tile + q_tile + 1023) & ~1023;
@@ -428,7 +434,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(full + i, 1);
-            mbar_init(empty + i, kvh);
+            mbar_init(empty + i, cwarps);
         }
         abort_flag = 0;
         fence_mbar_init();
@@ -448,7 +454,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
     const int nloc = (int)(hi - lo);
     if (nloc <= 0) return;
 
-    if (warp == kvh) {
+    if (warp == cwarps) {
         // ================= producer warp
         if (lane == 0) {
             prefetch_tmap(&tmap_k);
@@ -539,26 +545,38 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
         return;
     }
 
-    // ================= consumer warp kh: kv-head kh of the CTA's group
-    const int kh = warp;
+    // ================= consumer warp w: q-heads [hoff, hoff + gcount) of kv-head kh
+    // Products taken transposed, so that the 16 tokens of a block fill the M
+    // of m16n8k16 and up to 8 q-heads its N:
+    //   S^T (16 tokens x heads) = K Q^T and O^T (D x heads) += V^T P^T.
+    // Lane l holds heads 2(l%4) and 2(l%4)+1 (n) of tokens / dims l/4 and
+    // l/4+8 (m); the A operands are K (ldmatrix) and V^T (ldmatrix.trans), the
+    // B operands Q^T (registers, per sequence) and P^T (S^T's accumulators
+    // transposed by movmatrix).  A kv-head with more than 8 q-heads has several
+    // warps, each reading the same K/V tile.
+    const int kh = warp / p.wpk;
+    const int hoff = (warp - kh * p.wpk) * p.gw;
     const int G = p.group;
-    const int r = lane >> 2;        // query head row inside the m16 tile
-    const int quad = lane & 3;
-    const bool row_ok = r < G;
+    const int gcount = min(p.gw, G - hoff);
+    const int r = lane >> 2;        // token / dim row of the m16 fragments
+    const int quad = lane & 3;      // head columns 2*quad, 2*quad+1
+    const bool row_ok = r < gcount; // Q^T column r of the B fragments
+    const int h_first = kh * G + hoff;   // this warp's first q-head within the CTA's group
     // ldmatrix lane addressing inside one kv-head tile (128-byte rows, swizzled)
     const int mi = lane >> 3, rr = lane & 7;
     const int k_tok = ((mi >> 1) << 3) + rr, k_dsub = mi & 1;
     const int v_tok = ((mi & 1) << 3) + rr, v_dsub = mi >> 1;
+    constexpr int kMTiles = D / 16;
 
     int k = 0;
     while (k < nloc) {
         // ---- one piece: the blocks of one sequence (and kv-head group) in this slice;
         // its accumulators live only here, so the piece's end has registers to spare
-        float o[kNTiles][4];
-        uint32_t qa[kKSteps][2];
-        float m_run = -INFINITY, l_run = 0.f;
+        float ot[kMTiles][4];
+        uint32_t qb[kKSteps][2];
+        float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < kNTiles; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        for (int j = 0; j < kMTiles; ++j) ot[j][0] = ot[j][1] = ot[j][2] = ot[j][3] = 0.f;
         StageHeader h;
         int piece_lb0 = 0;
         bool aborted = false;
@@ -574,84 +592,73 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
             h = hdr[stage];
             const uint8_t *st = smem + (size_t)stage * stage_bytes;
             if (first_block) {
-                const uint8_t *qs = st + 2 * kv_tile + (size_t)(kh * G + r) * D * 2;
+                const uint8_t *qs = st + 2 * kv_tile + (size_t)(h_first + r) * D * 2;
 #pragma unroll
                 for (int ks = 0; ks < kKSteps; ++ks) {
-                    qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + quad * 2) * 2) : 0u;
-                    qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + 8 + quad * 2) * 2) : 0u;
+                    qb[ks][0] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + quad * 2) * 2) : 0u;
+                    qb[ks][1] = row_ok ? *reinterpret_cast<const uint32_t *>(qs + (ks * 16 + 8 + quad * 2) * 2) : 0u;
                 }
                 piece_lb0 = h.lb;
             }
             if (h.flags & kValid) {
                 const uint32_t kbase = smem_u32(st + kh * kHeadTileBytes);
                 const uint32_t vbase = smem_u32(st + kv_tile + kh * kHeadTileBytes);
-                // ---- S = Q K^T : two n-tiles of 8 tokens
-                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // ---- S^T = K Q^T: A = K (tokens x 16 dims per step), B = Q^T
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < kKSteps; ++ks) {
-                    const int chunk = ((ks & 3) << 1) + k_dsub;
-                    const uint32_t addr = kbase + (ks >> 2) * (kB * 128) + k_tok * 128 +
-                                          ((chunk ^ (k_tok & 7)) << 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(addr, b0, b1, b2, b3);
-                    mma_bf16_16816(sacc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-                    mma_bf16_16816(sacc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+                    const int chunk = ((ks & 3) << 1) + v_dsub;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kbase + (ks >> 2) * (kB * 128) + v_tok * 128 + ((chunk ^ (v_tok & 7)) << 4),
+                            a0, a1, a2, a3);
+                    mma_bf16_16816(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
-                // ---- online softmax on row r (tokens 2q, 2q+1, 8+2q, 9+2q)
+                // ---- online softmax per head column (heads 2q, 2q+1; tokens r, r+8)
                 const int ntok = h.ntok;
-                float x[2][2];
-                float tmax = -INFINITY;
+                float x[4];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int i = 0; i < 4; ++i) x[i] = (r + (i >> 1) * 8) < ntok ? s4[i] * p.scale_log2 : -INFINITY;
+                float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tok = nt * 8 + quad * 2 + e;
-                        const float val = tok < ntok ? sacc[nt][e] * p.scale_log2 : -INFINITY;
-                        x[nt][e] = val;
-                        tmax = fmaxf(tmax, val);
-                    }
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-                const float m_new = fmaxf(m_run, tmax);
-                if (m_new != -INFINITY) {
-                    const float alpha = fast_exp2(m_run - m_new);
-                    float pr[2][2];
-                    float psum = 0.f;
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                // ntok >= 1, so every column has a finite max
+                const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+                const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
+                const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
+                l_part[0] = l_part[0] * al0 + (p0 + p2);
+                l_part[1] = l_part[1] * al1 + (p1 + p3);
+                m_run[0] = mn0;
+                m_run[1] = mn1;
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
+                for (int j = 0; j < kMTiles; ++j) {
+                    ot[j][0] *= al0;
+                    ot[j][1] *= al1;
+                    ot[j][2] *= al0;
+                    ot[j][3] *= al1;
+                }
+                // P^T as the B operand: (token, head) pairs transposed to (head, token)
+                const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));   // tokens 0..7
+                const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));   // tokens 8..15
+                // masks for value rows past the sequence end (they may hold anything)
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (ntok < kB) {
+                    const int t0 = quad * 2;
+                    mlo = (t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u);
+                    mhi = (t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u);
+                }
+                // ---- O^T += V^T P^T: A = V^T (16 dims x 16 tokens per m-tile)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            pr[nt][e] = fast_exp2(x[nt][e] - m_new);
-                            psum += pr[nt][e];
-                        }
-                    l_run = l_run * alpha + psum;
-                    m_run = m_new;
-#pragma unroll
-                    for (int j = 0; j < kNTiles; ++j) {
-                        o[j][0] *= alpha;
-                        o[j][1] *= alpha;
-                    }
-                    const uint32_t pa0 = pack_bf16x2(pr[0][0], pr[0][1]);
-                    const uint32_t pa2 = pack_bf16x2(pr[1][0], pr[1][1]);
-                    // masks for value rows past the sequence end (they may hold anything)
-                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                    if (ntok < kB) {
-                        const int t0 = quad * 2;
-                        mlo = (t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u);
-                        mhi = (t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u);
-                    }
-                    // ---- O += P V : D/8 n-tiles of 8 dims, k = 16 tokens
-#pragma unroll
-                    for (int j2 = 0; j2 < kNTiles / 2; ++j2) {
-                        const int chunk = ((j2 & 3) << 1) + v_dsub;
-                        const uint32_t addr = vbase + (j2 >> 2) * (kB * 128) + v_tok * 128 +
-                                              ((chunk ^ (v_tok & 7)) << 4);
-                        uint32_t v0, v1, v2, v3;
-                        ldsm_x4_t(addr, v0, v1, v2, v3);
-                        v0 &= mlo; v2 &= mlo; v1 &= mhi; v3 &= mhi;
-                        mma_bf16_16816(o[2 * j2], pa0, 0u, pa2, 0u, v0, v1);
-                        mma_bf16_16816(o[2 * j2 + 1], pa0, 0u, pa2, 0u, v2, v3);
-                    }
+                for (int j = 0; j < kMTiles; ++j) {
+                    const int chunk = ((j & 3) << 1) + k_dsub;
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(vbase + (j >> 2) * (kB * 128) + k_tok * 128 + ((chunk ^ (k_tok & 7)) << 4),
+                              v0, v1, v2, v3);
+                    v0 &= mlo; v1 &= mlo; v2 &= mhi; v3 &= mhi;
+                    mma_bf16_16816(ot[j], v0, v1, v2, v3, pb0, pb1);
                 }
             }
             __syncwarp();
@@ -662,34 +669,45 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
         if (aborted) break;
 
         // ---- the piece's end
-        float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
-        l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-        const bool whole = piece_lb0 == 0 && (h.flags & kSeqEnd);
-        const int h_loc = kh * G + r;
-        const int64_t out_row = (int64_t)h.qrow * p.num_heads + (int64_t)h.hg * p.qh;
-        if (whole) {
-            if (row_ok) {
-                const float inv = 1.f / l_row;
-                __nv_bfloat16 *dst = p.out + (out_row + h_loc) * D + quad * 2;
+        float l0 = l_part[0], l1 = l_part[1];
 #pragma unroll
-                for (int j = 0; j < kNTiles; ++j)
-                    *reinterpret_cast<uint32_t *>(dst + j * 8) = pack_bf16x2(o[j][0] * inv, o[j][1] * inv);
-            }
-            continue;
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        // a piece of a sequence cut by CTA boundaries: store it, count it in;
-        // the warp that stores the last of the sequence's pieces merges them
+        const bool whole = piece_lb0 == 0 && (h.flags & kSeqEnd);
+        const int64_t out_row = (int64_t)h.qrow * p.num_heads + (int64_t)h.hg * p.qh;
         const int64_t vs = (int64_t)h.hg * S + h.seq;
         const int64_t slot = vs + blockIdx.x;
-        if (row_ok) {
-            float *dst = p.part_o + (slot * p.qh + h_loc) * D + quad * 2;
 #pragma unroll
-            for (int j = 0; j < kNTiles; ++j)
-                *reinterpret_cast<float2 *>(dst + j * 8) = make_float2(o[j][0], o[j][1]);
-            if (quad == 0)
-                *reinterpret_cast<float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2) = make_float2(m_run, l_row);
+        for (int e = 0; e < 2; ++e) {
+            const int hh = 2 * quad + e;
+            if (hh >= gcount) continue;
+            const int h_loc = h_first + hh;
+            const float l_e = e ? l1 : l0;
+            if (whole) {
+                const float inv = 1.f / l_e;
+                __nv_bfloat16 *dst = p.out + (out_row + h_loc) * D + r;
+#pragma unroll
+                for (int j = 0; j < kMTiles; ++j) {
+                    dst[j * 16] = __float2bfloat16_rn(ot[j][e] * inv);
+                    dst[j * 16 + 8] = __float2bfloat16_rn(ot[j][2 + e] * inv);
+                }
+            } else {
+                float *dst = p.part_o + (slot * p.qh + h_loc) * D + r;
+#pragma unroll
+                for (int j = 0; j < kMTiles; ++j) {
+                    dst[j * 16] = ot[j][e];
+                    dst[j * 16 + 8] = ot[j][2 + e];
+                }
+                if (r == 0)
+                    *reinterpret_cast<float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2) = make_float2(m_run[e], l_e);
+            }
         }
-        // (the stream's sizes are reloaded here rather than kept in registers through the loop)
+        if (whole) continue;
+        // a piece of a sequence cut by CTA boundaries, now stored: count it in;
+        // the warp that stores the last of the sequence's pieces merges them
+        // (the stream's sizes are reloaded here rather than kept in registers)
         const int64_t Tt = __ldg(p.prefix + S);
         const int64_t NVt = Tt * p.nhg;
         const int64_t Pt = p.shared_sms ? min((int64_t)gridDim.x, (int64_t)__ldg(p.active)) : (int64_t)gridDim.x;
@@ -703,12 +721,12 @@ __global__ void __launch_bounds__(32 * (kMaxKvhPerCta + 1), 1)
         }
         __syncwarp();   // every lane's stores precede lane 0's release
         int merge = 0;
-        if (lane == 0) merge = atomic_add_acq_rel_gpu(p.arrivals + c0 * kvh + kh, 1) == pieces - 1;
+        if (lane == 0) merge = atomic_add_acq_rel_gpu(p.arrivals + c0 * kMaxConsumerWarps + warp, 1) == pieces - 1;
         merge = __shfl_sync(0xffffffffu, merge, 0);   // (also orders lane 0's acquire before the loads)
         if (merge) {
-            for (int g = 0; g < G; g += 4)
-                merge_pieces<D>(p, vs, c0, c1, NVt, Pt, kh * G + g, G - g < 4 ? G - g : 4,
-                                p.out + (out_row + kh * G + g) * D);
+            for (int g = 0; g < gcount; g += 4)
+                merge_pieces<D>(p, vs, c0, c1, NVt, Pt, h_first + g, gcount - g < 4 ? gcount - g : 4,
+                                p.out + (out_row + h_first + g) * D);
         }
     }
 }
@@ -743,13 +761,19 @@ CUresult make_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int h
 }
 
 struct Layout {
-    int kvh, group, qh, nhg;
+    int kvh, wpk, gw, group, qh, nhg;
 };
 
+// kv-heads per CTA: up to 8 consumer warps of at most 8 q-heads each and up to
+// 32 q-heads in all, dividing the kv-heads evenly.
 Layout decode_layout(int num_heads, int num_kv_heads) {
     Layout L;
     L.group = num_heads / num_kv_heads;
-    int kvh = num_kv_heads < kMaxKvhPerCta ? num_kv_heads : kMaxKvhPerCta;
+    L.wpk = (L.group + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    L.gw = (L.group + L.wpk - 1) / L.wpk;
+    int kvh = kMaxConsumerWarps / L.wpk;
+    if (kvh > kMaxKvhPerCta) kvh = kMaxKvhPerCta;
+    if (kvh > num_kv_heads) kvh = num_kv_heads;
     while (kvh > 1 && (kvh * L.group > kMaxQHeadsPerCta || num_kv_heads % kvh != 0)) --kvh;
     L.kvh = kvh;
     L.qh = kvh * L.group;
@@ -760,7 +784,7 @@ Layout decode_layout(int num_heads, int num_kv_heads) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: the plan's prefix [S + 1] and SM split, the arrival counters of
-// cut sequences [kPartialCtas][kMaxKvhPerCta], the block stream [S * max_blocks],
+// cut sequences [kPartialCtas][kMaxConsumerWarps], the block stream [S * max_blocks],
 // then the partials, slot = hg*S + s + CTA (< NHG*S + CTAs): (m, l)
 // [slots][QH][2] and o [slots][QH][D], fp32.
 struct WorkspaceLayout {
@@ -773,7 +797,7 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
     w.prefix = 0;
     w.active = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 16);
     w.arrivals = align_up(w.active + sizeof(int32_t), 256);
-    w.stream = align_up(w.arrivals + sizeof(int32_t) * kPartialCtas * kMaxKvhPerCta, 256);
+    w.stream = align_up(w.arrivals + sizeof(int32_t) * kPartialCtas * kMaxConsumerWarps, 256);
     w.part_ml = align_up(w.stream + sizeof(StreamEntry) * (size_t)num_seqs * max_blocks, 256);
     w.part_o = align_up(w.part_ml + sizeof(float) * 2 * slots_heads, 256);
     w.total = align_up(w.part_o + sizeof(float) * (size_t)head_dim * slots_heads, 256);
@@ -790,7 +814,7 @@ cudaError_t launch_main(const DecodeParams &prm, const CUtensorMap &mk, const CU
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (timed) timing_begin(stream);
-    e = launch_dependent(kern, dim3(grid), dim3(32 * (prm.kvh + 1)), smem, stream, mk, mv, prm);
+    e = launch_dependent(kern, dim3(grid), dim3(32 * (prm.kvh * prm.wpk + 1)), smem, stream, mk, mv, prm);
     if (timed) timing_end(stream);
     return e;
 }
@@ -843,6 +867,8 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.num_seqs = a.num_seqs;
     prm.num_heads = a.num_heads;
     prm.kvh = L.kvh;
+    prm.wpk = L.wpk;
+    prm.gw = L.gw;
     prm.group = L.group;
     prm.qh = L.qh;
     prm.nhg = L.nhg;
@@ -894,7 +920,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     DecodeSplit split;
     split.active = reinterpret_cast<int32_t *>(ws + w.active);
     split.arrivals = prm.arrivals;
-    split.num_arrivals = grid * L.kvh;
+    split.num_arrivals = grid * kMaxConsumerWarps;
     split.grid = grid;
     split.share = share_sms ? 1 : 0;
     split.causal = a.causal;

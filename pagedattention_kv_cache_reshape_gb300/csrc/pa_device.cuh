@@ -37,6 +37,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held by the warp in the mma
+// fragment layout (lane l holds row l/4, columns 2(l%4) and 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // atomicAdd with acquire-release semantics at GPU scope: the caller's earlier
 // writes (and those ordered before it by a warp or CTA barrier) are visible
 // to whoever reads the new value, and the caller sees what was published

@@ -40,6 +40,22 @@ SMALL = {
     "mqa_small": lambda seed: W.build("mqa", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                       num_heads=8, num_kv_heads=1, head_dim=128, block_size=16,
                                       q_lens=[1] * 5, context_lens=[1, 17, 230, 64, 999], device=DEV),
+    # 16 q-heads per kv-head: two warps of 8 heads share each kv-head's K/V tiles
+    "g16_decode": lambda seed: W.build("g16d", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                       num_heads=32, num_kv_heads=2, head_dim=128, block_size=16,
+                                       q_lens=[1] * 6, context_lens=[3, 16, 161, 700, 48, 1200], device=DEV),
+    # 32 q-heads on one kv-head: four warps share its K/V tiles
+    "g32_decode": lambda seed: W.build("g32d", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                       num_heads=32, num_kv_heads=1, head_dim=128, block_size=16,
+                                       q_lens=[1] * 4, context_lens=[17, 300, 1, 520], device=DEV),
+    # 12 q-heads per kv-head (not a power of two): two warps of 6 heads each
+    "g12_decode": lambda seed: W.build("g12d", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                       num_heads=48, num_kv_heads=4, head_dim=64, block_size=16,
+                                       q_lens=[1] * 5, context_lens=[40, 16, 333, 2, 800], device=DEV),
+    # 2 q-heads per kv-head, 16 kv-heads (two kv-head groups of 8)
+    "g2_decode": lambda seed: W.build("g2d", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                      num_heads=32, num_kv_heads=16, head_dim=128, block_size=16,
+                                      q_lens=[1] * 5, context_lens=[1, 33, 250, 90, 640], device=DEV),
     "d64_bf16": lambda seed: W.build("d64", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                      num_heads=16, num_kv_heads=4, head_dim=64, block_size=16,
                                      q_lens=[1] * 7, context_lens=[5, 16, 33, 400, 2, 129, 1000], device=DEV),
