@@ -250,15 +250,13 @@ def run_ours(args, world, rank, local):
             pa.decode_step(q, key, value, w.k_cache, w.v_cache, bt, ctx, ss, cu, w.scale, out=o,
                            slot_mapping=slots, workspace=workspace, dev_status=status, stream=pa_stream)
             return
-        pa.compute_slot_mapping(bt, ss, cu, w.num_blocks, w.total_q, slot_mapping=slots,
-                                dev_status=status, stream=pa_stream)
-        pa.reshape_and_cache(key, value, w.k_cache, w.v_cache, slots, dev_status=status, stream=pa_stream)
-        pa.varlen_prefill(q, cu, w.k_cache, w.v_cache, bt, ctx, w.scale, max_q, out=o,
-                          workspace=workspace, dev_status=status, stream=pa_stream)
+        # slot mapping + cache write + varlen attention through the one-call step entry
+        pa.varlen_step(q, key, value, w.k_cache, w.v_cache, cu, bt, ctx, ss, w.scale, max_q, out=o,
+                       slot_mapping=slots, workspace=workspace, dev_status=status, stream=pa_stream)
 
-    # decode: plan (with the cache write), decode; mixed: slot mapping, cache
-    # write, plan (with the prefill plan), decode, prefill
-    launches_per_step = 2 if decode_only else 5
+    # decode: plan (with the cache write), decode; mixed: plan (with the cache
+    # write and the prefill plan), decode, prefill
+    launches_per_step = 2 if decode_only else 3
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()

@@ -272,6 +272,34 @@ PA_API pa_status pa_varlen_prefill(void *out, const void *q, const int32_t *cu_s
                             size_t workspace_bytes, int32_t *dev_status, pa_stream_t stream);
 
 /*
+ * One mixed continuous-batching step in one call ([iitog] model runner: the
+ * new tokens' K/V go into their cache slots, then attention over the
+ * super-sequence): exactly pa_compute_slot_mapping(block_tables, seq_start,
+ * cu_seqlens_q, total_q) -> slot_mapping, then pa_reshape_and_cache of key /
+ * value through it, then pa_varlen_prefill (same arguments, same results).
+ * The new tokens are the query tokens: token t of sequence s
+ * (cu_seqlens_q[s] <= t < cu_seqlens_q[s+1]) sits at position
+ * seq_start[s] + t - cu_seqlens_q[s], and context_lens[s] must count it.
+ * On the fast path (bf16, head_dim 64/128, 16-byte aligned rows and
+ * strides, decode and prefill kernels both applicable, max_q_len > 1) the
+ * slot mapping and the cache write run beside the attention's plan launch,
+ * saving two launches; otherwise the three calls run one after the other.
+ *  key, value   device [total_q][num_kv_heads][head_dim], token strides given
+ *  seq_start    device int32 [num_seqs]: tokens cached before this step
+ *  slot_mapping device int64 [total_q], written
+ *  workspace    >= pa_varlen_prefill_workspace_size(...) bytes, 16-byte aligned
+ */
+PA_API pa_status pa_varlen_step(void *out, const void *q, const void *key, const void *value,
+                                int64_t key_stride_tok, int64_t value_stride_tok, void *k_cache,
+                                void *v_cache, const int32_t *cu_seqlens_q,
+                                const int32_t *block_tables, const int32_t *context_lens,
+                                const int32_t *seq_start, int64_t *slot_mapping, int num_seqs,
+                                int total_q, int max_q_len, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size, int max_blocks, int num_blocks,
+                                float scale, pa_dtype dtype, void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, pa_stream_t stream);
+
+/*
  * Encode-only varlen paged attention: pa_varlen_prefill without the causal
  * mask.  Every query row of sequence s attends to all context_lens[s] keys of
  * s, and still to no other sequence's ("vLLMつかったら、ベクトル検索サーバーが

@@ -277,7 +277,7 @@ pa_status varlen_attention(void *out, const void *q, const int32_t *cu_seqlens_q
                            int num_heads, int num_kv_heads, int head_dim, int block_size,
                            int max_blocks, int num_blocks, float scale, pa_dtype dtype,
                            void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                           pa_stream_t stream, int causal) {
+                           pa_stream_t stream, int causal, const KvWriteArgs *write = nullptr) {
     pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                          max_blocks, num_blocks, dtype, scale);
     if (st != PA_OK) return st;
@@ -302,6 +302,23 @@ pa_status varlen_attention(void *out, const void *q, const int32_t *cu_seqlens_q
                                                              max_blocks);
         if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
     }
+    // the step's cache write (pa_varlen_step): beside the plan launch of the
+    // shared chain when its rows are 16-byte vectors, else ahead of attention
+    const bool fold_write = write && fast_decode && fast_prefill && max_q_len > 1 &&
+                            aligned(write->key, 16) && aligned(write->value, 16) &&
+                            (write->key_stride_tok * eb) % 16 == 0 && (write->value_stride_tok * eb) % 16 == 0 &&
+                            ((int64_t)num_kv_heads * head_dim * eb) % 16 == 0;
+    if (write && !fold_write) {
+        st = pa_compute_slot_mapping(block_tables, num_seqs, max_blocks, write->seq_start,
+                                     write->cu_seqlens_new, write->total_new, block_size, num_blocks,
+                                     write->slot_mapping, dev_status, stream);
+        if (st != PA_OK) return st;
+        st = pa_reshape_and_cache(write->key, write->value, write->key_stride_tok, write->value_stride_tok,
+                                  const_cast<void *>(k_cache), const_cast<void *>(v_cache), write->slot_mapping,
+                                  write->total_new, num_kv_heads, head_dim, block_size, num_blocks, dtype,
+                                  dev_status, stream);
+        if (st != PA_OK) return st;
+    }
     // decode rows (q_len == 1) stream through the split-KV decode kernels,
     // prefill chunks (q_len >= 2) through the tensor-core prefill kernel
     timing_begin(s);
@@ -317,7 +334,7 @@ pa_status varlen_attention(void *out, const void *q, const int32_t *cu_seqlens_q
         const std::function<cudaError_t()> prefill = [&]() {
             return launch_prefill_tc(a, pws, workspace_bytes - dec_ws, s, true);
         };
-        e = launch_split_decode(a, workspace, dec_ws, s, false, nullptr, &job, &prefill);
+        e = launch_split_decode(a, workspace, dec_ws, s, false, fold_write ? write : nullptr, &job, &prefill);
         timing_end(s);
         return from_cuda(e);
     }
@@ -364,6 +381,29 @@ pa_status pa_varlen_encode(void *out, const void *q, const int32_t *cu_seqlens_q
                             num_seqs, total_q, max_q_len, num_heads, num_kv_heads, head_dim,
                             block_size, max_blocks, num_blocks, scale, dtype, workspace,
                             workspace_bytes, dev_status, stream, 0);
+}
+
+pa_status pa_varlen_step(void *out, const void *q, const void *key, const void *value,
+                         int64_t key_stride_tok, int64_t value_stride_tok, void *k_cache, void *v_cache,
+                         const int32_t *cu_seqlens_q, const int32_t *block_tables,
+                         const int32_t *context_lens, const int32_t *seq_start, int64_t *slot_mapping,
+                         int num_seqs, int total_q, int max_q_len, int num_heads, int num_kv_heads,
+                         int head_dim, int block_size, int max_blocks, int num_blocks, float scale,
+                         pa_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                         pa_stream_t stream) {
+    pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                         max_blocks, num_blocks, dtype, scale);
+    if (st != PA_OK) return st;
+    if (total_q < 0 || max_q_len < 0) return PA_ERR_INVALID_ARG;
+    if (total_q == 0 || num_seqs == 0) return PA_OK;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (!key || !value || !seq_start || !cu_seqlens_q || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (key_stride_tok < row || value_stride_tok < row) return PA_ERR_INVALID_ARG;
+    const KvWriteArgs wr{key, value, key_stride_tok, value_stride_tok, seq_start, cu_seqlens_q,
+                         total_q, slot_mapping};
+    return varlen_attention(out, q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                            total_q, max_q_len, num_heads, num_kv_heads, head_dim, block_size, max_blocks,
+                            num_blocks, scale, dtype, workspace, workspace_bytes, dev_status, stream, 1, &wr);
 }
 
 pa_status pa_get_device_status(const int32_t *dev_status, int32_t *host_out, pa_stream_t stream) {

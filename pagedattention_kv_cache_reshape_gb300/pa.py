@@ -26,7 +26,7 @@ EXPORTS = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
     "pa_varlen_prefill_workspace_size", "pa_varlen_prefill", "pa_get_device_status",
     "pa_reset_device_status", "pa_set_timing_events", "pa_decode_static_scratch", "pa_decode_step",
-    "pa_copy_blocks", "pa_varlen_encode",
+    "pa_copy_blocks", "pa_varlen_encode", "pa_varlen_step",
     "pa_block_manager_create", "pa_block_manager_destroy", "pa_block_manager_num_free",
     "pa_block_manager_refcount", "pa_allocate_slots", "pa_free_sequence", "pa_share_prefix",
     "pa_block_manager_tables",
@@ -103,6 +103,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_decode_step.restype = i32
         L.pa_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                      i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]
+        L.pa_varlen_step.restype = i32
+        L.pa_varlen_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                     i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]
         L.pa_decode_static_scratch.restype = i32
         L.pa_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                                f32, i32, vp, vp]
@@ -304,6 +307,36 @@ def varlen_prefill(q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens
         _opt(dev_status), _stream(stream))
     _check(rc, "pa_varlen_prefill" if causal else "pa_varlen_encode")
     return out
+
+
+def varlen_step(q, key, value, k_cache, v_cache, cu_seqlens_q, block_tables, context_lens, seq_start,
+                scale: float, max_q_len: int, out=None, slot_mapping=None, workspace=None, dev_status=None,
+                stream=None):
+    """pa_varlen_step: slot mapping + cache write of the step's query tokens + causal varlen
+    attention over the super-sequence, in one call.  Returns (slot_mapping, out)."""
+    total_q, H, D = q.shape
+    num_blocks, block_size, hkv, d = k_cache.shape
+    num_seqs, max_blocks = block_tables.shape
+    for name, t in (("key", key), ("value", value)):
+        if t.dim() != 3 or t.shape[0] != total_q or t.shape[1:] != (hkv, d) or t.stride(2) != 1 \
+                or t.stride(1) != d:
+            raise ValueError(f"{name} must be [{total_q}, {hkv}, {d}] with contiguous rows")
+    if out is None:
+        out = torch.empty_like(q)
+    if slot_mapping is None:
+        slot_mapping = torch.empty(total_q, dtype=torch.int64, device=q.device)
+    need = varlen_prefill_workspace_size(num_seqs, total_q, H, hkv, D, block_size, max_blocks)
+    workspace = _ws(workspace, need, q.device)
+    rc = load().pa_varlen_step(
+        _contig(out, "out"), _contig(q, "q"), _dev(key, "key"), _dev(value, "value"), key.stride(0),
+        value.stride(0), _contig(k_cache, "k_cache"), _contig(v_cache, "v_cache"),
+        _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32), _contig(block_tables, "block_tables", torch.int32),
+        _contig(context_lens, "context_lens", torch.int32), _contig(seq_start, "seq_start", torch.int32),
+        _contig(slot_mapping, "slot_mapping", torch.int64), num_seqs, total_q, int(max_q_len), H, hkv, D,
+        block_size, max_blocks, num_blocks, float(scale), _dtype_code(q), _contig(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _opt(dev_status), _stream(stream))
+    _check(rc, "pa_varlen_step")
+    return slot_mapping, out
 
 
 def get_device_status(dev_status, stream=None) -> int:

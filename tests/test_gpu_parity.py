@@ -507,6 +507,49 @@ def test_fused_decode_step_token_strided_and_bad_slot():
     assert int(slots[s]) == -1
 
 
+def _varlen_step(w, key=None, value=None, **kw):
+    return pa.varlen_step(w.q, w.key if key is None else key, w.value if value is None else value,
+                          w.k_cache, w.v_cache, w.cu_seqlens_q, w.block_tables, w.context_lens, w.seq_start,
+                          w.scale, int(w.q_lens.max()), **kw)
+
+
+@pytest.mark.parametrize("name", ["mixed_small", "fp32_gqa_prefill", "gqa_small", "g12_decode"])
+def test_fused_varlen_step_equals_separate_calls(name):
+    """pa_varlen_step = slot mapping + cache write + varlen attention, bit for bit
+    (the write folded into the plan launch for mixed bf16 batches; separate
+    kernels for fp32 and for decode-only batches)."""
+    a = SMALL[name](13)
+    b = SMALL[name](13)
+    slots_a, out_a = gpu_step(a)
+    slots_b, out_b = _varlen_step(b)
+    torch.cuda.synchronize()
+    assert torch.equal(slots_a, slots_b)
+    bits = torch.int16 if a.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(a.k_cache.view(bits), b.k_cache.view(bits))
+    assert torch.equal(a.v_cache.view(bits), b.v_cache.view(bits))
+    assert torch.equal(out_a, out_b)
+
+
+def test_fused_varlen_step_full_size_mixed_and_strided():
+    """The full mixed step through pa_varlen_step equals the three calls bit for
+    bit, also with key / value as token-strided views of a fused QKV tensor."""
+    a = W.make("mixed_bf16", 0, oracle_blocks, device=DEV)
+    b = W.make("mixed_bf16", 0, oracle_blocks, device=DEV)
+    slots_a, out_a = gpu_step(a)
+    T, hkv, d = b.key.shape
+    fused = torch.empty(T, 3, hkv, d, dtype=b.dtype, device=DEV)
+    fused[:, 1] = b.key
+    fused[:, 2] = b.value
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots_b, out_b = _varlen_step(b, key=fused[:, 1], value=fused[:, 2], dev_status=status)
+    torch.cuda.synchronize()
+    assert pa.get_device_status(status) == 0
+    assert torch.equal(slots_a, slots_b)
+    assert torch.equal(a.k_cache.view(torch.int16), b.k_cache.view(torch.int16))
+    assert torch.equal(a.v_cache.view(torch.int16), b.v_cache.view(torch.int16))
+    assert torch.equal(out_a, out_b)
+
+
 def test_workspace_too_small_is_rejected():
     w = SMALL["gqa_small"](1)
     ws = torch.empty(64, dtype=torch.uint8, device=DEV)
