@@ -204,25 +204,6 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int b_mn_ma
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-
-// Same with the A operand read from tensor memory: M rows on the TMEM lanes,
-// K along the columns, two bf16 per 32-bit column (lower K index in bits
-// 0..15); a_tmem is the column of the first K element (lane field 0).
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-
 // Four chained MMAs over K = 64 (one 128-byte swizzled plane of both
 // operands): step k reads A and B 32 bytes further along their rows (the
 // descriptors' address field, in 16-byte units, advances by 2).  The first
@@ -243,8 +224,11 @@ __device__ __forceinline__ void umma_bf16_k64(uint32_t d_tmem, uint64_t a_desc, 
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(1u));
 }
 
-// Four chained MMAs with A from tensor memory over K = 64: step k reads A 8
-// columns (16 bf16 K values) further and B `b_step` (16-byte units) further.
+// Four chained MMAs with the A operand read from tensor memory, over K = 64:
+// A has its M rows on the TMEM lanes and K along the columns, two bf16 per
+// 32-bit column (lower K index in bits 0..15), a_tmem the column of the first
+// K element (lane field 0).  Step k reads A 8 columns (16 K values) further
+// and B `b_step` (16-byte units) further.
 __device__ __forceinline__ void umma_bf16_tmem_a_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                      uint32_t idesc, uint32_t b_step, uint32_t accumulate) {
     asm volatile(
