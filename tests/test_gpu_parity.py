@@ -147,6 +147,39 @@ def test_full_size_decode_every_output(name):
     _run_and_check_all(w)
 
 
+def test_many_sequences_decode_every_output():
+    """1500 decode rows: the plan scans its prefix in several passes of its CTA,
+    and most CTAs hold many whole sequences plus cut ones."""
+    rng = np.random.default_rng(77)
+    ctx = rng.integers(1, 200, size=1500)
+    w = W.build("many", seed=77, blocks_needed=oracle_blocks, dtype=torch.bfloat16, num_heads=16,
+                num_kv_heads=4, head_dim=128, block_size=16, q_lens=[1] * 1500, context_lens=ctx,
+                device=DEV)
+    _run_and_check_all(w)
+
+
+def test_many_decode_rows_in_a_mixed_step_every_output():
+    """2 prefill chunks among 1200 decode rows through pa_varlen_step: the
+    shared plan launch with its write CTAs over several scan passes, and the SM
+    split for a batch dominated by decode rows."""
+    rng = np.random.default_rng(78)
+    q_lens = np.ones(1202, dtype=np.int64)
+    q_lens[[17, 900]] = [96, 150]
+    ctx = rng.integers(1, 300, size=1202)
+    ctx[17], ctx[900] = 96 + 40, 150 + 333
+    w = W.build("many_mixed", seed=78, blocks_needed=oracle_blocks, dtype=torch.bfloat16, num_heads=32,
+                num_kv_heads=8, head_dim=128, block_size=16, q_lens=q_lens, context_lens=ctx, device=DEV)
+    wc = w.to("cpu")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots, out = pa.varlen_step(w.q, w.key, w.value, w.k_cache, w.v_cache, w.cu_seqlens_q, w.block_tables,
+                                w.context_lens, w.seq_start, w.scale, int(q_lens.max()), dev_status=status)
+    torch.cuda.synchronize()
+    assert pa.get_device_status(status) == 0
+    assert np.array_equal(slots.cpu().numpy(), oracle_write(wc))
+    assert torch.equal(w.k_cache.cpu().view(torch.int16), wc.k_cache.view(torch.int16))
+    compare(to_f64(out), oracle_attention(wc), w.dtype, "many_mixed")
+
+
 def test_full_size_mixed_sampled():
     w = W.make("mixed_bf16", 0, oracle_blocks, device=DEV)
     wc = _cpu_copy(w)
