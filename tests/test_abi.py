@@ -90,6 +90,20 @@ def test_host_validation_rejects_before_launch(lib):
     # prefill: null cu_seqlens_q
     assert L.pa_varlen_prefill(16, 16, nul, 16, 16, 16, 16, 2, 9, 8, 8, 4, 128, 16, 4, 8, 0.1, 1, 16, 1 << 20,
                                nul, nul) == pa.ERR_INVALID_ARG
+    # empty batches: nothing to do, nothing launched
+    assert L.pa_varlen_prefill(nul, nul, nul, nul, nul, nul, nul, 0, 0, 0, 8, 4, 128, 16, 4, 8, 0.1, 1, nul, 0,
+                               nul, nul) == pa.OK
+    assert L.pa_varlen_prefill(nul, nul, nul, nul, nul, nul, nul, 3, 0, 0, 8, 4, 128, 16, 4, 8, 0.1, 1, nul, 0,
+                               nul, nul) == pa.OK
+    assert L.pa_varlen_encode(nul, nul, nul, nul, nul, nul, nul, 0, 0, 0, 8, 4, 128, 16, 4, 8, 0.1, 1, nul, 0,
+                              nul, nul) == pa.OK
+    assert L.pa_varlen_step(nul, nul, nul, nul, 512, 512, nul, nul, nul, nul, nul, nul, nul, 0, 0, 0, 8, 4, 128,
+                            16, 4, 8, 0.1, 1, nul, 0, nul, nul) == pa.OK
+    assert L.pa_decode_step(nul, nul, nul, nul, 512, 512, nul, nul, nul, nul, nul, nul, 0, nul, 0, 8, 4, 128, 16,
+                            4, 8, 0.1, 1, nul, 0, nul, nul) == pa.OK
+    # varlen step: tokens to write but no key rows
+    assert L.pa_varlen_step(16, 16, nul, nul, 512, 512, 16, 16, 16, 16, 16, 16, 16, 2, 9, 8, 8, 4, 128, 16, 4,
+                            8, 0.1, 1, 16, 1 << 20, nul, nul) == pa.ERR_INVALID_ARG
     # status helpers: null pointers
     assert L.pa_get_device_status(nul, nul, nul) == pa.ERR_INVALID_ARG
     assert L.pa_reset_device_status(nul, nul) == pa.ERR_INVALID_ARG

@@ -180,6 +180,19 @@ def test_many_decode_rows_in_a_mixed_step_every_output():
     compare(to_f64(out), oracle_attention(wc), w.dtype, "many_mixed")
 
 
+@pytest.mark.parametrize("num_seqs", [16384, 16385])
+def test_largest_decode_batch_every_output(num_seqs):
+    """16384 sequences, the most the persistent decode kernel takes (the plan
+    keeps the whole prefix in 64 KB of shared memory); one more goes through
+    the generic kernel.  Short contexts keep the oracle quick."""
+    rng = np.random.default_rng(num_seqs)
+    ctx = rng.integers(1, 40, size=num_seqs)
+    w = W.build("largest", seed=num_seqs, blocks_needed=oracle_blocks, dtype=torch.bfloat16, num_heads=8,
+                num_kv_heads=2, head_dim=64, block_size=16, q_lens=[1] * num_seqs, context_lens=ctx,
+                device=DEV)
+    _run_and_check_all(w)
+
+
 def test_full_size_mixed_sampled():
     w = W.make("mixed_bf16", 0, oracle_blocks, device=DEV)
     wc = _cpu_copy(w)
