@@ -169,18 +169,27 @@ __global__ void __launch_bounds__(kPlanThreads)
     if (blockIdx.x == 0)
         for (int i = tid; i < split.num_arrivals; i += kPlanThreads) split.arrivals[i] = 0;
     if ((int)blockIdx.x >= job.first_cta) {
-        // ---- the step's cache write, beside the plan: one warp per new token
+        // ---- the step's cache write, beside the plan.  Work item = one chunk of
+        // up to 32 * kPre 16-byte vectors of one new token's K and V rows, so a
+        // wide row (32 kv-heads x 128 dims = 512 vectors) is spread over several
+        // warps and every warp's loads are in flight together before its stores.
         const int warps = kPlanThreads / 32;
         const int wctas = dgrid - job.first_cta;
-        constexpr int kPre = 4;   // 16-byte vectors per lane loaded before the slot is known
-        for (int t = ((int)blockIdx.x - job.first_cta) * warps + warp; t < job.total_new; t += wctas * warps) {
+        constexpr int kPre = 4;   // vectors per lane per item
+        constexpr int kChunk = 32 * kPre;
+        const int chunks = (job.row_vecs + kChunk - 1) / kChunk;
+        const int64_t items = (int64_t)job.total_new * chunks;
+        for (int64_t it = (int64_t)((int)blockIdx.x - job.first_cta) * warps + warp; it < items;
+             it += (int64_t)wctas * warps) {
+            const int t = (int)(it / chunks);
+            const int v0 = (int)(it - (int64_t)t * chunks) * kChunk;
             const uint4 *ks = job.key + t * job.key_stride_v;
             const uint4 *vs = job.value + t * job.value_stride_v;
             // the rows depend only on t: their loads overlap the slot's dependent loads
             uint4 kr[kPre], vr[kPre];
 #pragma unroll
             for (int u = 0; u < kPre; ++u) {
-                const int i = lane + 32 * u;
+                const int i = v0 + lane + 32 * u;
                 if (i < job.row_vecs) {
                     kr[u] = __ldg(ks + i);
                     vr[u] = __ldg(vs + i);
@@ -209,14 +218,18 @@ __global__ void __launch_bounds__(kPlanThreads)
                 }
                 const int64_t pos = (int64_t)st + (t - c0);
                 const int64_t logical = pos / kB;
+                // every chunk of the token finds the same slot; the first records it
                 if (pos < 0 || logical >= max_blocks) {
-                    set_status(status, PA_ERR_OUT_OF_RANGE);
+                    if (v0 == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
                 } else {
                     const int32_t phys = __ldg(block_tables + (int64_t)s * max_blocks + logical);
-                    if (phys < 0 || phys >= num_blocks) set_status(status, PA_ERR_OUT_OF_RANGE);
-                    else slot = (int64_t)phys * kB + (pos - logical * kB);
+                    if (phys < 0 || phys >= num_blocks) {
+                        if (v0 == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
+                    } else {
+                        slot = (int64_t)phys * kB + (pos - logical * kB);
+                    }
                 }
-                job.slot_mapping[t] = slot;
+                if (v0 == 0) job.slot_mapping[t] = slot;
             }
             slot = __shfl_sync(0xffffffffu, slot, 0);
             if (slot < 0 || slot >= job.pool_slots) continue;
@@ -224,17 +237,11 @@ __global__ void __launch_bounds__(kPlanThreads)
             uint4 *vd = job.v_cache + slot * job.row_vecs;
 #pragma unroll
             for (int u = 0; u < kPre; ++u) {
-                const int i = lane + 32 * u;
+                const int i = v0 + lane + 32 * u;
                 if (i < job.row_vecs) {
                     kd[i] = kr[u];
                     vd[i] = vr[u];
                 }
-            }
-            for (int i = lane + 32 * kPre; i < job.row_vecs; i += 32) {
-                const uint4 kv = __ldg(ks + i);
-                const uint4 vv = __ldg(vs + i);
-                kd[i] = kv;
-                vd[i] = vv;
             }
         }
         return;
@@ -931,7 +938,10 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
     if (plan_grid > 2 * sms) plan_grid = 2 * sms;
     if (plan_grid < 1) plan_grid = 1;
-    int write_grid = write ? (write->total_new + kPlanThreads / 32 - 1) / (kPlanThreads / 32) : 0;
+    // write items: a new token's row in chunks of 128 16-byte vectors, one warp each
+    const int64_t write_items =
+        write ? (int64_t)write->total_new * ((job.row_vecs + 127) / 128) : 0;
+    int write_grid = (int)((write_items + kPlanThreads / 32 - 1) / (kPlanThreads / 32));
     if (write_grid > 2 * sms) write_grid = 2 * sms;
     job.first_cta = plan_grid;
     plan_grid += write_grid;                    // + the CTAs of the cache write

@@ -76,11 +76,26 @@ __global__ void reshape_and_cache_kernel(const char *__restrict__ key,
     const V *vs = reinterpret_cast<const V *>(value + t * value_stride_b);
     V *kd = reinterpret_cast<V *>(k_cache) + slot * row_vecs;
     V *vd = reinterpret_cast<V *>(v_cache) + slot * row_vecs;
-    for (int i = lane; i < row_vecs; i += 32) {
-        const V kv = __ldg(ks + i);
-        const V vv = __ldg(vs + i);
-        kd[i] = kv;
-        vd[i] = vv;
+    // four vectors of K and of V per lane in flight before their stores
+    constexpr int kBatch = 4;
+    for (int i0 = lane; i0 < row_vecs; i0 += 32 * kBatch) {
+        V kv[kBatch], vv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + 32 * u;
+            if (i < row_vecs) {
+                kv[u] = __ldg(ks + i);
+                vv[u] = __ldg(vs + i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + 32 * u;
+            if (i < row_vecs) {
+                kd[i] = kv[u];
+                vd[i] = vv[u];
+            }
+        }
     }
 }
 
