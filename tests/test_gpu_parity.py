@@ -56,6 +56,11 @@ SMALL = {
     "g2_decode": lambda seed: W.build("g2d", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                       num_heads=32, num_kv_heads=16, head_dim=128, block_size=16,
                                       q_lens=[1] * 5, context_lens=[1, 33, 250, 90, 640], device=DEV),
+    # 12 kv-heads x 128 dims: a token row of 192 16-byte vectors, written by the step's
+    # cache write as one full chunk of 128 and a ragged one of 64
+    "row192_decode": lambda seed: W.build("r192", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                          num_heads=24, num_kv_heads=12, head_dim=128, block_size=16,
+                                          q_lens=[1] * 6, context_lens=[1, 16, 17, 300, 95, 700], device=DEV),
     "d64_bf16": lambda seed: W.build("d64", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                      num_heads=16, num_kv_heads=4, head_dim=64, block_size=16,
                                      q_lens=[1] * 7, context_lens=[5, 16, 33, 400, 2, 129, 1000], device=DEV),
@@ -499,7 +504,8 @@ def test_stale_workspace_contents_do_not_matter(name):
     assert torch.equal(clean, dirty)
 
 
-@pytest.mark.parametrize("name", ["gqa_small", "tiny", "long_small", "mha_small", "mqa_small", "d64_bf16"])
+@pytest.mark.parametrize("name", ["gqa_small", "tiny", "long_small", "mha_small", "mqa_small", "d64_bf16",
+                                  "g2_decode", "row192_decode"])
 def test_fused_decode_step_equals_separate_calls(name):
     """pa_decode_step = slot mapping + cache write + decode, bit for bit."""
     a = SMALL[name](12)
@@ -529,13 +535,14 @@ def test_fused_decode_step_full_size_matches_oracle():
     compare(to_f64(out), oracle_attention(wc), torch.bfloat16, "decode step gqa256")
 
 
-def test_fused_decode_step_token_strided_and_bad_slot():
-    w = SMALL["gqa_small"](14)
+@pytest.mark.parametrize("name", ["gqa_small", "mha_small"])
+def test_fused_decode_step_token_strided_and_bad_slot(name):
+    w = SMALL[name](14)
     T, hkv, d = w.key.shape
     fused = torch.empty(T, 3, hkv, d, dtype=w.dtype, device=DEV)
     fused[:, 1] = w.key
     fused[:, 2] = w.value
-    ref = SMALL["gqa_small"](14)
+    ref = SMALL[name](14)
     _, out_ref = gpu_step(ref)
     _, out = pa.decode_step(w.q, fused[:, 1], fused[:, 2], w.k_cache, w.v_cache, w.block_tables,
                             w.context_lens, w.seq_start, w.cu_seqlens_q, w.scale)
