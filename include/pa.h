@@ -361,6 +361,33 @@ PA_API pa_status pa_block_manager_tables(pa_block_manager *m, const int64_t *seq
                                          int32_t *num_tokens);
 
 /*
+ * Host-side check of the preconditions the kernels rely on but do not test,
+ * for tests and debug runs.  All pointers are HOST memory; nothing touches
+ * the device.  [kwkr] §1.2-1.3: a sequence reaches its blocks through its
+ * block table, block i of a sequence holding its tokens i*B..i*B+B-1, and
+ * blocks may be referenced read-only by several tables (a shared prefix).
+ *  block_tables  int32 [num_seqs][max_blocks]; only the first
+ *                ceil(context_lens[s] / block_size) entries of row s are used
+ *  context_lens  int32 [num_seqs], or NULL to skip checks 1-2 and 5
+ *  slot_mapping  int64 [num_slots] (the slots a write will fill), or NULL
+ * Checks, in this order (the first failure is reported):
+ *   1 every context_lens[s] is in [1, max_blocks * block_size];
+ *   2 every used table entry is in [0, num_blocks);
+ *   3 every slot is < num_blocks * block_size (negative slots are padding);
+ *   4 no slot appears twice;
+ *   5 no slot lies in a block that two or more used table entries reference
+ *     (a shared block is read-only; writing it needs copy-on-write).
+ * Returns PA_OK; PA_ERR_OUT_OF_RANGE for checks 1-3; PA_ERR_INVALID_ARG for
+ * checks 4-5 or bad sizes.  *failed_check (1-5, 0 when OK) and *bad_index
+ * (the offending row of context_lens or block_tables, or the index into
+ * slot_mapping) are set when non-NULL.
+ */
+PA_API pa_status pa_validate_inputs(const int32_t *block_tables, int num_seqs, int max_blocks,
+                                    const int32_t *context_lens, const int64_t *slot_mapping,
+                                    int num_slots, int block_size, int num_blocks,
+                                    int *failed_check, int64_t *bad_index);
+
+/*
  * Copies the device status word to *host_out after synchronising `stream`.
  * Returns PA_ERR_CUDA if the copy fails (for example after a sticky fault).
  */

@@ -29,7 +29,7 @@ EXPORTS = (
     "pa_copy_blocks", "pa_varlen_encode", "pa_varlen_step",
     "pa_block_manager_create", "pa_block_manager_destroy", "pa_block_manager_num_free",
     "pa_block_manager_refcount", "pa_allocate_slots", "pa_free_sequence", "pa_share_prefix",
-    "pa_block_manager_tables",
+    "pa_block_manager_tables", "pa_validate_inputs",
 )
 STATIC_SCRATCH_BYTES = 24 << 20
 
@@ -109,6 +109,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_decode_static_scratch.restype = i32
         L.pa_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                                f32, i32, vp, vp]
+        L.pa_validate_inputs.restype = i32
+        L.pa_validate_inputs.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int64)]
         _lib = L
         return L
 
@@ -337,6 +340,30 @@ def varlen_step(q, key, value, k_cache, v_cache, cu_seqlens_q, block_tables, con
         workspace.numel() * workspace.element_size(), _opt(dev_status), _stream(stream))
     _check(rc, "pa_varlen_step")
     return slot_mapping, out
+
+
+def validate_inputs(block_tables, context_lens, slot_mapping, block_size: int, num_blocks: int):
+    """pa_validate_inputs on host (CPU) tensors.  Returns (status, check, index):
+    status PA_OK or the error code, check the failed check (1-5, 0 when OK) and
+    index the offending row or slot index (-1 when OK).  context_lens and
+    slot_mapping may be None."""
+    def host(t, dtype, name):
+        if t is None:
+            return None, None
+        t = torch.as_tensor(t)
+        if t.device.type != "cpu" or t.dtype != dtype:
+            raise TypeError(f"{name}: expected a CPU {dtype} tensor")
+        t = t.contiguous()
+        return t, t.data_ptr()
+    bt, bt_p = host(block_tables, torch.int32, "block_tables")
+    ctx, ctx_p = host(context_lens, torch.int32, "context_lens")
+    sl, sl_p = host(slot_mapping, torch.int64, "slot_mapping")
+    num_seqs, max_blocks = (bt.shape[0], bt.shape[1]) if bt is not None else (0, 0)
+    check, index = ctypes.c_int(-1), ctypes.c_int64(-2)
+    rc = load().pa_validate_inputs(bt_p, num_seqs, max_blocks, ctx_p, sl_p,
+                                   0 if sl is None else sl.numel(), block_size, num_blocks,
+                                   ctypes.byref(check), ctypes.byref(index))
+    return int(rc), int(check.value), int(index.value)
 
 
 def get_device_status(dev_status, stream=None) -> int:
