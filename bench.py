@@ -174,6 +174,26 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle (CPU) sample
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: the
+    implementer and part codes), with the machine type."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return f"{fields['model name']} ({platform.machine()})"
+    if "CPU part" in fields:
+        return f"{platform.machine()} CPU implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.machine() or "unknown"
+
+
 def oracle_sample(w_cpu: W.Workload, budget_s: float, nthreads: int, repeat: bool = False):
     """Times the oracle, as it stands, on a prefix of the workload's sequences
     sized to about `budget_s`.  With `repeat`, a sample that is the whole
@@ -551,6 +571,7 @@ def main():
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "tokens_per_s": round(world * w.total_q * K / total_s, 1),
+        "context_tokens_per_s": round(world * b["logical_tokens"] * K / total_s, 1),
         "kv_gbs_logical": round(b["kv_logical"] * K * world / total_s / 1e9, 2),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
         "pct_of_nominal_8tbs": round(100 * gbs / world / 8000.0, 2),
@@ -592,9 +613,14 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         import oracle as O
         nthreads = os.cpu_count() or 1
-        bps, secs, desc, n, _ = oracle_sample(w.to("cpu"), args.cpu_seconds, nthreads, repeat=True)
+        w_cpu = w.to("cpu")
+        bps, secs, desc, n, _ = oracle_sample(w_cpu, args.cpu_seconds, nthreads, repeat=True)
+        bps1, secs1, desc1, _, _ = oracle_sample(w_cpu, args.cpu_seconds / 4, 1)
         line["cpu_baseline"] = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": nthreads,
-                                "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+                                "kind": "oracle", "sample": desc, "seconds": round(secs, 2),
+                                "cpu_model": cpu_model(),
+                                "single_thread": {"value": round(bps1 / 1e9, 4), "unit": "GB/s",
+                                                  "sample": desc1, "seconds": round(secs1, 2)}}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -673,7 +699,7 @@ def main_reference(args, world, rank):
         "data": "synthetic (seeded N(0,1) values, power-law lengths, shuffled block pool)",
         "config": {"workload": w.name, "sample_sequences": n, "num_seqs": w.num_seqs},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
