@@ -101,6 +101,14 @@ struct DecodeParams {
     int tma_heads; // kv-heads per TMA op (kvh, or 1 with the per-head map)
     float scale_log2;
     int32_t *status;
+    // for the L2 prefetch of the CTA's first blocks while it waits for the
+    // plan (decode calls without cu_seqlens_q only; null context_lens: none)
+    const int32_t *context_lens;
+    const int32_t *block_tables;
+    int max_blocks;
+    int num_blocks;
+    int num_kv_heads;
+    const uint8_t *k_bytes, *v_bytes;   // the pools
 };
 
 // Optional cache write folded into the plan kernel (pa_decode_step): for new
@@ -418,6 +426,81 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t vs, 
     }
 }
 
+// ------------------------------------------------------------------ early prefetch
+// While the decode CTA waits for the plan, it finds the first blocks of its
+// own slice from context_lens and the block tables (the same partition the
+// plan builds: the blocks of all sequences in order, cut into P equal slices)
+// and prefetches them into L2, so the first copies after the wait hit L2.  A
+// prefetch is only a hint: it reads inputs before the wait, and a stale value
+// would cost time, never a wrong result.  All threads of the CTA take part;
+// warp_tot is shared memory for one int per warp.
+template <int D>
+__device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int nblocks, int32_t *warp_tot) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = blockDim.x;
+    const int S = p.num_seqs;
+    const int64_t max_tok = (int64_t)p.max_blocks * kB;
+    // 1. blocks of this thread's contiguous range of sequences
+    const int s0 = (int)((int64_t)S * tid / nthr), s1 = (int)((int64_t)S * (tid + 1) / nthr);
+    int sum = 0;
+    for (int s = s0; s < s1; ++s) {
+        const int ctx = __ldg(p.context_lens + s);
+        if (ctx >= 1 && ctx <= max_tok) sum += (ctx + kB - 1) / kB;
+    }
+    // 2. exclusive prefix over the threads' ranges
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0, T = 0;
+    for (int w = 0; w < nthr / 32; ++w) {
+        const int t = warp_tot[w];
+        if (w < warp) before += t;
+        T += t;
+    }
+    const int excl = before + incl - sum;
+    if (T <= 0 || sum == 0) return;
+    // 3. the slice's first nblocks entries: the thread whose range holds one walks to it
+    const int64_t NV = (int64_t)T * p.nhg, P = gridDim.x;
+    const int64_t lo = (int64_t)blockIdx.x * NV / P, hi = ((int64_t)blockIdx.x + 1) * NV / P;
+    const int64_t row_bytes = (int64_t)p.num_kv_heads * D * 2;       // one token of all kv-heads
+    const uint32_t span = (uint32_t)(p.kvh * D * 2);                 // the kv-heads of one group
+    for (int k = 0; k < nblocks; ++k) {
+        const int64_t v = lo + k;
+        if (v >= hi) break;
+        const int hg = (int)(v / T);
+        const int b = (int)(v - (int64_t)hg * T);
+        if (b < excl || b >= excl + sum) continue;
+        int acc = excl;
+        for (int s = s0; s < s1; ++s) {
+            const int ctx = __ldg(p.context_lens + s);
+            const int nb = (ctx >= 1 && ctx <= max_tok) ? (ctx + kB - 1) / kB : 0;
+            if (b < acc + nb) {
+                const int32_t blk = __ldg(p.block_tables + (int64_t)s * p.max_blocks + (b - acc));
+                if (blk >= 0 && blk < p.num_blocks) {
+                    const int64_t base = (int64_t)blk * kB * row_bytes;
+                    if (p.nhg == 1) {
+                        prefetch_l2_bulk(p.k_bytes + base, (uint32_t)(kB * row_bytes));
+                        prefetch_l2_bulk(p.v_bytes + base, (uint32_t)(kB * row_bytes));
+                    } else {
+                        const int64_t off = base + (int64_t)hg * span;
+                        for (int t = 0; t < kB; ++t) {
+                            prefetch_l2_bulk(p.k_bytes + off + t * row_bytes, span);
+                            prefetch_l2_bulk(p.v_bytes + off + t * row_bytes, span);
+                        }
+                    }
+                }
+                break;
+            }
+            acc += nb;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ main kernel
 template <int D>
 __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
@@ -438,6 +521,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(hdr + NS);
     uint64_t *empty = full + NS;
     __shared__ int abort_flag;
+    __shared__ int32_t pf_warp_tot[kMaxConsumerWarps + 1];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -450,6 +534,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
+    if (p.context_lens) prefetch_first_blocks<D>(p, NS, pf_warp_tot);
     grid_dependency_wait();      // the plan (and everything before it) is complete
     grid_dependents_launch();    // the next kernel may become resident
 
@@ -887,6 +972,16 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim);
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.status = a.status;
+    // decode calls (one query row per sequence, all CTAs take a slice): each
+    // CTA prefetches its first blocks into L2 while it waits for the plan
+    const bool early = !share_sms && a.cu_seqlens_q == nullptr;
+    prm.context_lens = early ? a.context_lens : nullptr;
+    prm.block_tables = a.block_tables;
+    prm.max_blocks = a.max_blocks;
+    prm.num_blocks = a.num_blocks;
+    prm.num_kv_heads = a.num_kv_heads;
+    prm.k_bytes = static_cast<const uint8_t *>(a.k_cache);
+    prm.v_bytes = static_cast<const uint8_t *>(a.v_cache);
 
     // tensor maps: one TMA per block for all kv-heads of the CTA
     CUtensorMap mk, mv;
