@@ -432,12 +432,14 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t vs, 
 // plan builds: the blocks of all sequences in order, cut into P equal slices)
 // and prefetches them into L2, so the first copies after the wait hit L2.  A
 // prefetch is only a hint: it reads inputs before the wait, and a stale value
-// would cost time, never a wrong result.  All threads of the CTA take part;
-// warp_tot is shared memory for one int per warp.
+// would cost time, never a wrong result.  Threads [0, nthr) take part (the
+// consumer warps: the producer goes straight on to its wait and first
+// copies); they meet at named barrier 1.  warp_tot is shared memory for one
+// int per warp.
 template <int D>
-__device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int nblocks, int32_t *warp_tot) {
+__device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int nblocks, int32_t *warp_tot,
+                                                      int nthr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthr = blockDim.x;
     const int S = p.num_seqs;
     const int64_t max_tok = (int64_t)p.max_blocks * kB;
     // 1. blocks of this thread's contiguous range of sequences
@@ -455,7 +457,7 @@ __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int
         if (lane >= off) incl += y;
     }
     if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
+    asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
     int before = 0, T = 0;
     for (int w = 0; w < nthr / 32; ++w) {
         const int t = warp_tot[w];
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
-    if (p.context_lens) prefetch_first_blocks<D>(p, NS, pf_warp_tot);
+    if (p.context_lens && warp < cwarps) prefetch_first_blocks<D>(p, NS, pf_warp_tot, 32 * cwarps);
     grid_dependency_wait();      // the plan (and everything before it) is complete
     grid_dependents_launch();    // the next kernel may become resident
 
