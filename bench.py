@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--next-rows", action="store_true",
+                    help="measure the NEXT rows instead (block fork / swap / pack, encode-only "
+                         "attention, host block allocator): one JSON line each")
     return ap.parse_args()
 
 
@@ -239,6 +242,160 @@ def oracle_sample(w_cpu: W.Workload, budget_s: float, nthreads: int, repeat: boo
             + (f", run {reps} times" if reps > 1 else "")
             + f", slot mapping + cache write + attention, fp64 oracle, {nthreads} threads")
     return total / t, t, desc, n, ws
+
+
+# ------------------------------------------------------------------ NEXT rows
+
+def run_next_rows(args):
+    """One JSON line per NEXT row, each against its roofline:
+      f1 fork      pa_copy_blocks inside one device pool (HBM: read + write);
+      f1 swap out  device pool -> pinned host pool, f1 swap in: back (the host
+                   link; beside it the copy engine's rate for the same bytes);
+      f4 pack      pool -> contiguous device buffer, f4 unpack: back (HBM);
+      f3 encode    pa_varlen_encode, 8 chunks of 512 rows over 0-2048 cached
+                   tokens, non-causal (tensor pipe);
+      f2 allocator pa_allocate_slots for a 256-sequence decode step (host).
+    Pools are shaped like the decode workloads' (16 tokens x 8 kv-heads x 128
+    dims bf16: 32 KB a block a pool); block ids are seeded random permutations.
+    Device timings: CUDA events on the launching stream, L2 flushed before
+    each call, median of 20."""
+    from pagedattention_kv_cache_reshape_gb300 import build, pa
+    build.build()
+    pa.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peaks()
+    tc_peak = measured_tflops()
+    rng = np.random.default_rng(args.seed)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    evict = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    evict_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def timed(fn, reps=20, warm=3):
+        ts = []
+        for i in range(reps + warm):
+            flush.zero_()
+            torch.sum(evict, dim=0, out=evict_sum)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= warm:
+                ts.append(a.elapsed_time(b) / 1e3)
+        return float(np.median(ts))
+
+    def emit(row, value, unit, roofline, config):
+        print(json.dumps({"row": row, "value": round(value, 2), "unit": unit, "roofline": roofline,
+                          "config": config, "data": "synthetic (seeded)"}), flush=True)
+
+    def hbm_roof(nbytes, secs):
+        ach = nbytes / secs / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "bytes_per_call": int(nbytes), "ms": round(secs * 1e3, 4)}
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    nblk, npairs = 8192, 2048
+    shape = (nblk, 16, 8, 128)
+    k = torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+    block_bytes = 16 * 8 * 128 * 2
+    perm = rng.permutation(nblk).astype(np.int32)
+    src, dst = perm[:npairs], perm[npairs:2 * npairs]           # distinct, and no destination is a source
+    cfg = {"pool_blocks": nblk, "pairs": npairs, "block": "16 x 8 x 128 bf16 (32 KB a pool)"}
+
+    # f1 fork inside one pool
+    fork = torch.from_numpy(np.stack([src, dst], 1)).to(dev)
+    t = timed(lambda: pa.copy_blocks(k, v, k, v, fork, dev_status=status))
+    nbytes = npairs * 2 * block_bytes * 2
+    emit("f1 fork (block copy inside the device pool)", nbytes / t / 1e9, "GB/s", hbm_roof(nbytes, t), cfg)
+
+    # f4 pack to / unpack from a contiguous buffer
+    buf_k = torch.empty((npairs,) + shape[1:], dtype=torch.bfloat16, device=dev)
+    buf_v = torch.empty_like(buf_k)
+    seq = np.arange(npairs, dtype=np.int32)
+    pack = torch.from_numpy(np.stack([src, seq], 1)).to(dev)
+    unpack = torch.from_numpy(np.stack([seq, dst], 1)).to(dev)
+    t = timed(lambda: pa.copy_blocks(k, v, buf_k, buf_v, pack, dev_status=status))
+    emit("f4 pack (pool blocks to a contiguous transfer buffer)", nbytes / t / 1e9, "GB/s", hbm_roof(nbytes, t), cfg)
+    t = timed(lambda: pa.copy_blocks(buf_k, buf_v, k, v, unpack, dev_status=status))
+    emit("f4 unpack (transfer buffer to pool blocks)", nbytes / t / 1e9, "GB/s", hbm_roof(nbytes, t), cfg)
+
+    # f1 swap out / in through a pinned host pool, beside the copy engine on the same bytes
+    host_k = torch.empty((npairs,) + shape[1:], dtype=torch.bfloat16).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
+    one_way = npairs * 2 * block_bytes
+    t_out = timed(lambda: pa.copy_blocks(k, v, host_k, host_v, pack, dev_status=status))
+    t_in = timed(lambda: pa.copy_blocks(host_k, host_v, k, v, unpack, dev_status=status))
+    t_ce_out = timed(lambda: (host_k.copy_(buf_k, non_blocking=True), host_v.copy_(buf_v, non_blocking=True)))
+    t_ce_in = timed(lambda: (buf_k.copy_(host_k, non_blocking=True), buf_v.copy_(host_v, non_blocking=True)))
+    for row, tt, tce in (("f1 swap out (device pool to pinned host pool)", t_out, t_ce_out),
+                         ("f1 swap in (pinned host pool to device pool)", t_in, t_ce_in)):
+        ach, ce = one_way / tt / 1e9, one_way / tce / 1e9
+        emit(row, ach, "GB/s", {"bound": "host link", "achieved": round(ach, 1), "peak": round(ce, 1),
+                                "unit": "GB/s", "frac": round(ach / ce, 4),
+                                "peak_source": "the copy engine moving the same bytes contiguously (measured here)",
+                                "bytes_per_call": one_way, "ms": round(tt * 1e3, 4)}, cfg)
+    torch.cuda.synchronize()
+    if pa.get_device_status(status) != 0:
+        raise RuntimeError("device status set by a block copy")
+
+    # f3 encode-only attention on mixed-step-shaped chunks
+    w = W.mixed(args.seed, pa.num_blocks_needed, num_decode=0, device=dev)
+    q_lens = (w.cu_seqlens_q[1:] - w.cu_seqlens_q[:-1]).cpu().numpy()
+    ctx = w.context_lens.cpu().numpy()
+    flops = float(sum(4 * w.num_heads * w.head_dim * int(ql) * int(c) for ql, c in zip(q_lens, ctx)))
+    out = torch.empty_like(w.q)
+    ws = torch.empty(pa.varlen_prefill_workspace_size(w.num_seqs, w.total_q, w.num_heads, w.num_kv_heads,
+                                                      w.head_dim, w.block_size, w.max_blocks),
+                     dtype=torch.uint8, device=dev)
+    t = timed(lambda: pa.varlen_prefill(w.q, w.cu_seqlens_q, w.k_cache, w.v_cache, w.block_tables,
+                                        w.context_lens, w.scale, int(q_lens.max()), out=out, workspace=ws,
+                                        causal=False))
+    ach = flops / t / 1e12
+    emit("f3 encode-only varlen attention", ach, "TFLOP/s",
+         {"bound": "tensor", "achieved": round(ach, 1), "peak": tc_peak, "unit": "TFLOP/s",
+          "frac": round(ach / tc_peak, 4), "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops)",
+          "flops_per_call": flops, "ms": round(t * 1e3, 4)},
+         {"chunks": int(len(q_lens)), "rows": int(w.total_q), "context_tokens": int(ctx.sum()),
+          "heads": f"{w.num_heads} q / {w.num_kv_heads} kv", "head_dim": w.head_dim})
+
+    # f2 host allocator: one decode step of 256 sequences (one new token each)
+    g = W.make("gqa256_bf16", args.seed, pa.num_blocks_needed, device="cpu")
+    steps = 200
+    lens = [int(c) for c in g.context_lens.tolist()]
+    need = sum(pa.num_blocks_needed(c + steps, 16) for c in lens)
+    m = pa.BlockManager(need + 256, 16, pa.num_blocks_needed(max(lens) + steps, 16))
+    for s_, c in enumerate(lens):
+        if m.allocate_slots(s_, c - 1) != pa.OK:
+            raise RuntimeError("allocator: prompt allocation failed")
+    bad = 0
+    ids = np.arange(g.num_seqs, dtype=np.int64)
+    ones = np.ones(g.num_seqs, dtype=np.int32)
+    half = steps // 2
+    t0 = time.perf_counter()
+    for _ in range(half):                       # one pa_allocate_slots_batch call a step
+        bad += m.allocate_slots_batch(ids, ones) != pa.OK
+    dt_batch = (time.perf_counter() - t0) / half
+    t0 = time.perf_counter()
+    for _ in range(steps - half):               # one pa_allocate_slots call a sequence
+        for s_ in range(g.num_seqs):
+            bad += m.allocate_slots(s_, 1) != pa.OK
+    dt_each = (time.perf_counter() - t0) / (steps - half)
+    m.close()
+    if bad:
+        raise RuntimeError("allocator: a decode-step allocation failed")
+    emit("f2 host allocator (allocate_slots, one token for each of 256 sequences)", dt_batch * 1e6,
+         "us per step",
+         {"bound": "host", "us_per_sequence": round(dt_batch * 1e6 / g.num_seqs, 4),
+          "one_call_per_sequence_us_per_step": round(dt_each * 1e6, 2),
+          "note": "value: one pa_allocate_slots_batch call a step through the Python binding; beside it, "
+                  "one pa_allocate_slots call a sequence"},
+         {"sequences": g.num_seqs, "steps": steps})
 
 
 # ------------------------------------------------------------------ our path
@@ -527,6 +684,8 @@ def main():
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
     if args.impl == "reference":
         return main_reference(args, world, rank)
+    if args.next_rows:
+        return run_next_rows(args)
 
     r = run_ours(args, world, rank, local)
     w = r["w"]

@@ -343,6 +343,15 @@ PA_API int pa_block_manager_refcount(pa_block_manager *m, int block);
  * into a shared block would need copy-on-write, which is not provided).
  */
 PA_API pa_status pa_allocate_slots(pa_block_manager *m, int64_t seq_id, int num_new_tokens);
+/*
+ * allocate_slots for n sequences in one call, in order, under one lock (a
+ * decode step grows every running sequence by a token).  statuses[i]
+ * (nullable) receives what pa_allocate_slots(m, seq_ids[i],
+ * num_new_tokens[i]) returns.  Returns PA_OK when all succeed, else the
+ * first failure's status; PA_ERR_INVALID_ARG for a NULL manager or arrays.
+ */
+PA_API pa_status pa_allocate_slots_batch(pa_block_manager *m, const int64_t *seq_ids,
+                                         const int32_t *num_new_tokens, int n, int32_t *statuses);
 /* Drops seq_id's references; blocks no table references go back to the pool. */
 PA_API pa_status pa_free_sequence(pa_block_manager *m, int64_t seq_id);
 /*

@@ -61,9 +61,9 @@ int pa_block_manager_num_free(pa_block_manager *m) {
     return (int)m->free_queue.size();
 }
 
-pa_status pa_allocate_slots(pa_block_manager *m, int64_t seq_id, int num_new_tokens) {
-    if (!m || num_new_tokens < 0) return PA_ERR_INVALID_ARG;
-    std::lock_guard<std::mutex> lock(m->mu);
+// allocate_slots with the manager's lock held
+static pa_status allocate_locked(pa_block_manager *m, int64_t seq_id, int num_new_tokens) {
+    if (num_new_tokens < 0) return PA_ERR_INVALID_ARG;
     pa_block_manager::Seq &s = m->seqs[seq_id];
     const int64_t total = s.num_tokens + num_new_tokens;
     const int64_t need = blocks_for(total, m->block_size) - (int64_t)s.blocks.size();
@@ -88,6 +88,25 @@ pa_status pa_allocate_slots(pa_block_manager *m, int64_t seq_id, int num_new_tok
     }
     s.num_tokens = total;
     return PA_OK;
+}
+
+pa_status pa_allocate_slots(pa_block_manager *m, int64_t seq_id, int num_new_tokens) {
+    if (!m) return PA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(m->mu);
+    return allocate_locked(m, seq_id, num_new_tokens);
+}
+
+pa_status pa_allocate_slots_batch(pa_block_manager *m, const int64_t *seq_ids, const int32_t *num_new_tokens,
+                                  int n, int32_t *statuses) {
+    if (!m || n < 0 || (n > 0 && (!seq_ids || !num_new_tokens))) return PA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(m->mu);
+    pa_status first = PA_OK;
+    for (int i = 0; i < n; ++i) {
+        const pa_status st = allocate_locked(m, seq_ids[i], num_new_tokens[i]);
+        if (statuses) statuses[i] = st;
+        if (st != PA_OK && first == PA_OK) first = st;
+    }
+    return first;
 }
 
 pa_status pa_free_sequence(pa_block_manager *m, int64_t seq_id) {

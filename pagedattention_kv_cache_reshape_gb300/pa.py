@@ -29,7 +29,7 @@ EXPORTS = (
     "pa_copy_blocks", "pa_varlen_encode", "pa_varlen_step",
     "pa_block_manager_create", "pa_block_manager_destroy", "pa_block_manager_num_free",
     "pa_block_manager_refcount", "pa_allocate_slots", "pa_free_sequence", "pa_share_prefix",
-    "pa_block_manager_tables", "pa_validate_inputs",
+    "pa_block_manager_tables", "pa_validate_inputs", "pa_allocate_slots_batch",
 )
 STATIC_SCRATCH_BYTES = 24 << 20
 
@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_block_manager_refcount.argtypes = [vp, i32]
         L.pa_allocate_slots.restype = i32
         L.pa_allocate_slots.argtypes = [vp, i64, i32]
+        L.pa_allocate_slots_batch.restype = i32
+        L.pa_allocate_slots_batch.argtypes = [vp, vp, vp, i32, vp]
         L.pa_free_sequence.restype = i32
         L.pa_free_sequence.argtypes = [vp, i64]
         L.pa_share_prefix.restype = i32
@@ -440,6 +442,23 @@ class BlockManager:
     def allocate_slots(self, seq_id: int, num_new_tokens: int) -> int:
         """Returns the status (OK, ERR_OUT_OF_RANGE when the pool is short, ...)."""
         return int(self._L.pa_allocate_slots(self._h, int(seq_id), int(num_new_tokens)))
+
+    def allocate_slots_batch(self, seq_ids, num_new_tokens, statuses=None) -> int:
+        """pa_allocate_slots_batch on host int64 seq_ids / int32 counts (numpy
+        or CPU tensors); fills statuses (int32, same length) when given."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        cnt = np.ascontiguousarray(num_new_tokens, dtype=np.int32)
+        if ids.shape != cnt.shape:
+            raise ValueError("seq_ids and num_new_tokens must have the same length")
+        st_ptr = None
+        if statuses is not None:
+            if not (isinstance(statuses, np.ndarray) and statuses.dtype == np.int32 and statuses.flags.c_contiguous
+                    and statuses.shape == ids.shape):
+                raise ValueError("statuses must be a contiguous int32 numpy array of the same length")
+            st_ptr = statuses.ctypes.data
+        return int(self._L.pa_allocate_slots_batch(self._h, ids.ctypes.data, cnt.ctypes.data, int(ids.size),
+                                                   st_ptr))
 
     def free(self, seq_id: int) -> int:
         return int(self._L.pa_free_sequence(self._h, int(seq_id)))

@@ -128,3 +128,33 @@ def test_batch_from_the_manager_feeds_the_slot_mapping():
     for s in ids:
         own = set(bt[s][bt[s] >= 0].tolist())
         assert {int(x) // 16 for x in slots[cu[s]:cu[s + 1]]} <= own
+
+
+def test_batched_allocation_equals_one_call_per_sequence():
+    """pa_allocate_slots_batch = pa_allocate_slots in order: the same statuses
+    (including a pool running dry part-way and a shared last block) and the
+    same block tables."""
+    rng = np.random.default_rng(11)
+    a = pa.BlockManager(40, 16, max_blocks_per_seq=32)
+    b = pa.BlockManager(40, 16, max_blocks_per_seq=32)
+    for m in (a, b):
+        assert m.allocate_slots(0, 32) == pa.OK          # two whole blocks
+        assert m.share_prefix(0, 1, 32) == pa.OK         # seq 1 shares them
+        assert m.allocate_slots(2, 20) == pa.OK
+        assert m.share_prefix(2, 3, 16) == pa.OK         # seq 3 shares block 0 of seq 2
+    ids = np.array([5, 6, 0, 1, 2, 7, 3, 8, 9, 5], dtype=np.int64)
+    cnt = rng.integers(0, 200, ids.size).astype(np.int32)
+    cnt[4] = 3                                           # seq 2 appends into its own partial block
+    want = [a.allocate_slots(int(s), int(n)) for s, n in zip(ids, cnt)]
+    got = np.full(ids.size, -1, dtype=np.int32)
+    first = b.allocate_slots_batch(ids, cnt, got)
+    assert got.tolist() == want
+    assert first == next((x for x in want if x != pa.OK), pa.OK)
+    assert pa.ERR_OUT_OF_RANGE in want                   # the pool ran dry part-way
+    # sequences that exist: the four set up, and those with an allocation that succeeded
+    all_ids = sorted({int(s) for s, st in zip(ids, want) if st == pa.OK} | {0, 1, 2, 3})
+    ta, na = a.tables(all_ids, 32)
+    tb, nb = b.tables(all_ids, 32)
+    assert np.array_equal(ta, tb) and np.array_equal(na, nb)
+    assert a.num_free == b.num_free
+    assert b.allocate_slots_batch(np.zeros(0, np.int64), np.zeros(0, np.int32)) == pa.OK
