@@ -3,8 +3,8 @@
 
 One step = one pass of the whole path over one batch of synthetic input:
 slot mapping -> KV-cache write of the step's new tokens -> paged attention
-(decode: the split-KV kernel, which merges the pieces of cut sequences itself; mixed batches: decode rows plus prefill
-chunks).  The default workload is the batch-256 GQA decode configuration
+(decode: the split-KV kernel, which merges the pieces of cut sequences
+itself; mixed batches: decode rows plus prefill chunks).  The default workload is the batch-256 GQA decode configuration
 (32 q-heads / 8 kv-heads, head_dim 128, bf16, block size 16, context lengths
 from a power law x^-1.2 on [16, 4096], 64 sequences sharing a 1024-token
 prefix).
