@@ -55,6 +55,7 @@ constexpr int kMaxQHeadsPerCta = 32;
 constexpr int kHeadsPerWarp = 8;    // the N of one m16n8k16 product: q-heads per consumer warp
 constexpr int kMaxGroup = 32;       // q-heads per kv-head
 constexpr int kMaxSeqs = 16384;     // prefix of all sequences kept in shared memory
+constexpr int kMaxSeqsEarlyPrefetch = 4096;   // the early prefetch reads every context length: bounded
 constexpr int kPartialCtas = 512;   // partial slots reserved for CTA boundaries
 constexpr int kPlanThreads = 256;
 constexpr int kSmemBudget = 227 * 1024;
@@ -445,9 +446,13 @@ __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int
     // 1. blocks of this thread's contiguous range of sequences
     const int s0 = (int)((int64_t)S * tid / nthr), s1 = (int)((int64_t)S * (tid + 1) / nthr);
     int sum = 0;
-    for (int s = s0; s < s1; ++s) {
-        const int ctx = __ldg(p.context_lens + s);
-        if (ctx >= 1 && ctx <= max_tok) sum += (ctx + kB - 1) / kB;
+    for (int s = s0; s < s1; s += 8) {          // eight loads in flight at a time
+        int c[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) c[u] = s + u < s1 ? __ldg(p.context_lens + s + u) : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (c[u] >= 1 && c[u] <= max_tok) sum += (c[u] + kB - 1) / kB;
     }
     // 2. exclusive prefix over the threads' ranges
     int incl = sum;
@@ -976,7 +981,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.status = a.status;
     // decode calls (one query row per sequence, all CTAs take a slice): each
     // CTA prefetches its first blocks into L2 while it waits for the plan
-    const bool early = !share_sms && a.cu_seqlens_q == nullptr;
+    const bool early = !share_sms && a.cu_seqlens_q == nullptr && a.num_seqs <= kMaxSeqsEarlyPrefetch;
     prm.context_lens = early ? a.context_lens : nullptr;
     prm.block_tables = a.block_tables;
     prm.max_blocks = a.max_blocks;
