@@ -61,6 +61,14 @@ SMALL = {
     "row192_decode": lambda seed: W.build("r192", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                           num_heads=24, num_kv_heads=12, head_dim=128, block_size=16,
                                           q_lens=[1] * 6, context_lens=[1, 16, 17, 300, 95, 700], device=DEV),
+    # a single sequence: one token (one block for the whole grid), and a long one
+    # (every CTA a slice of the same sequence, merged from 152 pieces)
+    "one_token": lambda seed: W.build("one1", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                      num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                                      q_lens=[1], context_lens=[1], device=DEV),
+    "one_long": lambda seed: W.build("oneL", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                     num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                                     q_lens=[1], context_lens=[9000], device=DEV),
     "d64_bf16": lambda seed: W.build("d64", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                      num_heads=16, num_kv_heads=4, head_dim=64, block_size=16,
                                      q_lens=[1] * 7, context_lens=[5, 16, 33, 400, 2, 129, 1000], device=DEV),
@@ -505,7 +513,7 @@ def test_stale_workspace_contents_do_not_matter(name):
 
 
 @pytest.mark.parametrize("name", ["gqa_small", "tiny", "long_small", "mha_small", "mqa_small", "d64_bf16",
-                                  "g2_decode", "row192_decode"])
+                                  "g2_decode", "row192_decode", "one_token", "one_long"])
 def test_fused_decode_step_equals_separate_calls(name):
     """pa_decode_step = slot mapping + cache write + decode, bit for bit."""
     a = SMALL[name](12)
