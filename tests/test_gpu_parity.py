@@ -69,6 +69,10 @@ SMALL = {
     "one_long": lambda seed: W.build("oneL", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                      num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                                      q_lens=[1], context_lens=[9000], device=DEV),
+    # one 131,072-token sequence: 8,192 blocks, every CTA a slice of it, one merge of all pieces
+    "one_128k": lambda seed: W.build("one128k", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                     num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                                     q_lens=[1], context_lens=[131072], device=DEV),
     "d64_bf16": lambda seed: W.build("d64", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                      num_heads=16, num_kv_heads=4, head_dim=64, block_size=16,
                                      q_lens=[1] * 7, context_lens=[5, 16, 33, 400, 2, 129, 1000], device=DEV),
