@@ -429,98 +429,91 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t vs, 
 
 // ------------------------------------------------------------------ tree merge
 // A sequence cut into many pieces (a few long sequences spread over all
-// CTAs) is merged pairwise, up a fixed binary tree over its pieces' local
-// indices i = c - c0 (0..n-1), as the pieces arrive: at level l the pair
-// (left = k 2^{l+1}, right = left + 2^l) has one counter; the warp that
-// arrives second merges right into left's slot (the rule of merge_pieces
-// for two pieces, left first) and goes on up, so only about log2(n) merges
-// follow the last piece instead of n.  The tree is fixed, so results do not
-// depend on which piece arrives first.  Counters: the unit's pair j (pairs
-// counted level by level) at c0 + j < c1, so units never share one.  Each
-// level costs a counter round trip and a pair of partials (about 2 us on
-// GB300), so below about 64 pieces the single merge of all pieces by the last
-// arrival (two pieces' loads in flight) is faster (measured: 38 pieces, 12 us
-// slower by the tree; 76 pieces, 2 us faster; 152 pieces, 27 us faster).
-constexpr int kTreeMinPieces = 64;
+// CTAs) is merged up a fixed 4-ary tree over its pieces' local indices
+// i = c - c0 (0..n-1), as the pieces arrive: at level l the group g holds the
+// children g 4^{l+1} + m 4^l (m = 0..3, those < n) and one counter; the warp
+// that brings the counter to the group's child count merges the children in
+// order into the first child's slot (merge_pieces' online rule) and goes on
+// up, so about log4(n) merges follow the last piece instead of n.  The tree
+// is fixed, so results do not depend on which piece arrives first.
+// Counters: the unit's group j (groups with two or more children, counted
+// level by level) at c0 + j < c1, so units never share one.
+constexpr int kTreeMinPieces = 16;
+constexpr int kTreeFan = 4;
 
-// pairs at levels below l of a tree over n leaves
-__device__ __forceinline__ int tree_pairs_below(int l, int n) {
-    int j = 0;
-    for (int m = 0; m < l; ++m) {
-        const int span = 1 << m;
-        if (n > span) j += (n - span + 2 * span - 1) >> (m + 1);
-    }
-    return j;
+// groups with two or more children at level m of the tree over n leaves
+__device__ __forceinline__ int tree_groups(int m, int n) {
+    const int child = 1 << (2 * m), span = child << 2;   // 4^m, 4^{m+1}
+    return n > child ? (n - child + span - 1) / span : 0;
 }
 
-// Right's partial (m, l, o) merged into left's slot, for nh <= 4 q-heads h0..
+// Children base, base + stride, ... (cnt of them, slots vs + c0 + index) merged
+// in order for nh <= 4 q-heads h0..; into the first child's slot, or, with
+// `dst`, normalised into the output rows.
 template <int D>
-__device__ __forceinline__ void merge_pair(const DecodeParams &p, int64_t sl, int64_t sr, int h0, int nh) {
+__device__ __forceinline__ void merge_group(const DecodeParams &p, int64_t slot0, int stride, int cnt, int h0,
+                                            int nh, __nv_bfloat16 *dst) {
     constexpr int kPer = D / 32;
+    constexpr int kH = 4;
     const int lane = threadIdx.x & 31;
+    float M[kH], L[kH], acc[kH][kPer];
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
-        if (hh >= nh) break;
-        const int h = h0 + hh;
-        const float2 a = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (sl * p.qh + h) * 2));
-        const float2 b = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (sr * p.qh + h) * 2));
-        float *ol = p.part_o + (sl * p.qh + h) * D + lane * kPer;
-        const float *orr = p.part_o + (sr * p.qh + h) * D + lane * kPer;
-        float vl[kPer], vr[kPer];
-        if constexpr (kPer == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(ol));
-            const float4 y = __ldcg(reinterpret_cast<const float4 *>(orr));
-            vl[0] = x.x; vl[1] = x.y; vl[2] = x.z; vl[3] = x.w;
-            vr[0] = y.x; vr[1] = y.y; vr[2] = y.z; vr[3] = y.w;
-        } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2 *>(ol));
-            const float2 y = __ldcg(reinterpret_cast<const float2 *>(orr));
-            vl[0] = x.x; vl[1] = x.y;
-            vr[0] = y.x; vr[1] = y.y;
-        }
-        // (the same online rule as merge_pieces: left is the running value)
-        float M = a.x, Lsum = a.y;
-        float acc[kPer];
+    for (int hh = 0; hh < kH; ++hh) {
+        M[hh] = -INFINITY;
+        L[hh] = 0.f;
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) acc[u] = vl[u];
-        if (a.x == -INFINITY) {
-            M = b.x; Lsum = b.y;
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) acc[u] = vr[u];
-        } else if (b.x != -INFINITY) {
-            const float Mn = fmaxf(a.x, b.x);
-            const float fa = fast_exp2(a.x - Mn), fb = fast_exp2(b.x - Mn);
-            Lsum = a.y * fa + b.y * fb;
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) acc[u] = vl[u] * fa + vr[u] * fb;
-            M = Mn;
-        }
-        if constexpr (kPer == 4) {
-            *reinterpret_cast<float4 *>(ol) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        } else {
-            *reinterpret_cast<float2 *>(ol) = make_float2(acc[0], acc[1]);
-        }
-        if (lane == 0) *reinterpret_cast<float2 *>(p.part_ml + (sl * p.qh + h) * 2) = make_float2(M, Lsum);
+        for (int u = 0; u < kPer; ++u) acc[hh][u] = 0.f;
     }
-}
-
-// The merged slot normalised into the output rows, for nh <= 4 q-heads h0..
-template <int D>
-__device__ __forceinline__ void store_merged(const DecodeParams &p, int64_t sl, int h0, int nh,
-                                             __nv_bfloat16 *dst) {
-    constexpr int kPer = D / 32;
-    const int lane = threadIdx.x & 31;
+    for (int k0 = 0; k0 < cnt; k0 += 2) {
+        float2 ml[2][kH];
+        float ov[2][kH][kPer];
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
+        for (int k = 0; k < 2; ++k) {
+            const int64_t slot = slot0 + (int64_t)(k0 + k < cnt ? k0 + k : k0) * stride;
+#pragma unroll
+            for (int hh = 0; hh < kH; ++hh) {
+                const int h_loc = h0 + (hh < nh ? hh : 0);
+                ml[k][hh] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (slot * p.qh + h_loc) * 2));
+                const float *src = p.part_o + (slot * p.qh + h_loc) * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                    ov[k][hh][0] = t.x; ov[k][hh][1] = t.y; ov[k][hh][2] = t.z; ov[k][hh][3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                    ov[k][hh][0] = t.x; ov[k][hh][1] = t.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int hh = 0; hh < kH; ++hh) {
+                if (k0 + k >= cnt || ml[k][hh].x == -INFINITY) continue;
+                const float Mn = fmaxf(M[hh], ml[k][hh].x);
+                const float a = fast_exp2(M[hh] - Mn), b = fast_exp2(ml[k][hh].x - Mn);
+                L[hh] = L[hh] * a + ml[k][hh].y * b;
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) acc[hh][u] = acc[hh][u] * a + ov[k][hh][u] * b;
+                M[hh] = Mn;
+            }
+    }
+#pragma unroll
+    for (int hh = 0; hh < kH; ++hh) {
         if (hh >= nh) break;
-        const int h = h0 + hh;
-        const float2 a = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (sl * p.qh + h) * 2));
-        const float *src = p.part_o + (sl * p.qh + h) * D + lane * kPer;
-        const float inv = 1.f / a.y;
+        if (dst) {
+            const float inv = 1.f / L[hh];
 #pragma unroll
-        for (int u = 0; u < kPer; u += 2) {
-            const float2 x = __ldcg(reinterpret_cast<const float2 *>(src + u));
-            *reinterpret_cast<uint32_t *>(dst + hh * D + lane * kPer + u) = pack_bf16x2(x.x * inv, x.y * inv);
+            for (int u = 0; u < kPer; u += 2)
+                *reinterpret_cast<uint32_t *>(dst + hh * D + lane * kPer + u) =
+                    pack_bf16x2(acc[hh][u] * inv, acc[hh][u + 1] * inv);
+        } else {
+            float *o = p.part_o + (slot0 * p.qh + h0 + hh) * D + lane * kPer;
+            if constexpr (kPer == 4) {
+                *reinterpret_cast<float4 *>(o) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+            } else {
+                *reinterpret_cast<float2 *>(o) = make_float2(acc[hh][0], acc[hh][1]);
+            }
+            if (lane == 0) *reinterpret_cast<float2 *>(p.part_ml + (slot0 * p.qh + h0 + hh) * 2) = make_float2(M[hh], L[hh]);
         }
     }
 }
@@ -914,27 +907,28 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         const int64_t c0 = cta_of(h.hg * Tt + b0, NVt, Pt), c1 = cta_of(h.hg * Tt + b1 - 1, NVt, Pt);
         int pieces = (int)(c1 - c0 + 1);
         if (NVt >= Pt && pieces >= kTreeMinPieces) {
-            // many pieces (no slice is empty here): pairwise, up the sequence's tree
+            // many pieces (no slice is empty here): group by group, up the sequence's tree
             int node = (int)((int64_t)blockIdx.x - c0);
-            bool second = true;
-            for (int l = 0; (1 << l) < pieces; ++l) {
-                const int left = (node >> (l + 1)) << (l + 1), right = left + (1 << l);
-                if (right >= pieces) continue;   // no partner at this level: up unchanged
-                const int j = tree_pairs_below(l, pieces) + (node >> (l + 1));
-                __syncwarp();   // every lane's stores precede lane 0's release
-                int got = 0;
-                if (lane == 0) got = atomic_add_acq_rel_gpu(p.arrivals + (c0 + j) * kMaxConsumerWarps + warp, 1);
-                second = __shfl_sync(0xffffffffu, got, 0) == 1;   // (orders the acquire before the loads)
-                if (!second) break;   // the partner arrives second and merges
-                for (int g = 0; g < gcount; g += 4)
-                    merge_pair<D>(p, vs + c0 + left, vs + c0 + right, h_first + g, gcount - g < 4 ? gcount - g : 4);
-                node = left;
-            }
-            if (second) {   // the root
-                __syncwarp();
-                for (int g = 0; g < gcount; g += 4)
-                    store_merged<D>(p, vs + c0, h_first + g, gcount - g < 4 ? gcount - g : 4,
-                                    p.out + (out_row + h_first + g) * D);
+            bool last = true;
+            int base = 0;   // groups at the levels below
+            for (int l = 0; (1 << (2 * l)) < pieces; ++l) {
+                const int child = 1 << (2 * l), span = child * kTreeFan;
+                const int g = node / span, first = g * span;
+                const int cnt = min(kTreeFan, (pieces - first + child - 1) / child);
+                if (cnt >= 2) {
+                    __syncwarp();   // every lane's stores precede lane 0's release
+                    int got = 0;
+                    if (lane == 0) got = atomic_add_acq_rel_gpu(p.arrivals + (c0 + base + g) * kMaxConsumerWarps + warp, 1);
+                    last = __shfl_sync(0xffffffffu, got, 0) == cnt - 1;   // (orders the acquire before the loads)
+                    if (!last) break;   // a later child merges the group
+                    const bool root = span >= pieces;
+                    for (int h = 0; h < gcount; h += 4)
+                        merge_group<D>(p, vs + c0 + first, child, cnt, h_first + h, gcount - h < 4 ? gcount - h : 4,
+                                       root ? p.out + (out_row + h_first + h) * D : nullptr);
+                    if (root) break;
+                }
+                node = first;
+                base += tree_groups(l, pieces);
             }
             continue;
         }
