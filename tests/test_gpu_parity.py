@@ -337,6 +337,20 @@ def test_run_to_run_determinism():
         assert torch.equal(o, a)
 
 
+@pytest.mark.parametrize("name", ["one_long", "one_128k"])
+def test_many_piece_merge_is_deterministic(name):
+    """One sequence over every CTA: its pieces merge up a fixed tree in whatever
+    order they arrive; repeated calls and a stale workspace give the same bits."""
+    w = SMALL[name](3)
+    _, a = gpu_step(w)
+    ws_bytes = pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, 16, w.max_blocks)
+    for fill in (0x00, 0xFF, 0x5A):
+        ws = torch.full((ws_bytes,), fill, dtype=torch.uint8, device=DEV)
+        o = pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(o, a)
+
+
 def _mixed_for_streams():
     w = W.mixed(4, oracle_blocks, num_prefill=4, chunk=300, prefix_hi=900, num_decode=60, dec_lo=20,
                 dec_hi=1500, device=DEV)
