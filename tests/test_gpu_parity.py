@@ -73,6 +73,14 @@ SMALL = {
     "one_128k": lambda seed: W.build("one128k", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                      num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                                      q_lens=[1], context_lens=[131072], device=DEV),
+    # one long MHA sequence: four kv-head groups, each cut over a quarter of the CTAs (tree merges)
+    "one_long_mha": lambda seed: W.build("oneLm", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                         num_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
+                                         q_lens=[1], context_lens=[20000], device=DEV),
+    # one long sequence with 16 q-heads per kv-head: two warps per kv-head, each its own tree
+    "one_long_g16": lambda seed: W.build("oneLg", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
+                                         num_heads=32, num_kv_heads=2, head_dim=64, block_size=16,
+                                         q_lens=[1], context_lens=[40000], device=DEV),
     "d64_bf16": lambda seed: W.build("d64", seed=seed, blocks_needed=oracle_blocks, dtype=torch.bfloat16,
                                      num_heads=16, num_kv_heads=4, head_dim=64, block_size=16,
                                      q_lens=[1] * 7, context_lens=[5, 16, 33, 400, 2, 129, 1000], device=DEV),
@@ -337,7 +345,7 @@ def test_run_to_run_determinism():
         assert torch.equal(o, a)
 
 
-@pytest.mark.parametrize("name", ["one_long", "one_128k"])
+@pytest.mark.parametrize("name", ["one_long", "one_128k", "one_long_mha", "one_long_g16"])
 def test_many_piece_merge_is_deterministic(name):
     """One sequence over every CTA: its pieces merge up a fixed tree in whatever
     order they arrive; repeated calls and a stale workspace give the same bits."""
