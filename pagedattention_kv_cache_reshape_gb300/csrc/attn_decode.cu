@@ -497,6 +497,7 @@ __device__ __forceinline__ void merge_group(const DecodeParams &p, int64_t slot0
                 M[hh] = Mn;
             }
     }
+    __syncwarp();   // every lane's loads of the children precede the first child's overwrite
 #pragma unroll
     for (int hh = 0; hh < kH; ++hh) {
         if (hh >= nh) break;
