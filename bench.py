@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="gqa256_bf16", choices=list(W.FULL_CONFIGS))
+    ap.add_argument("--config", default="gqa256_bf16", choices=list(W.FULL_CONFIGS) + list(W.EXTRA_CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true", help="launch each step's kernels directly")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU sample")

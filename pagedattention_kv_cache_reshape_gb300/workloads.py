@@ -245,5 +245,18 @@ FULL_CONFIGS = {
 }
 
 
+def long_single(seed: int, blocks_needed: BlocksNeeded, device="cpu") -> Workload:
+    """One 131,072-token sequence (8,192 blocks; every decode CTA takes a slice
+    of it), otherwise as the long-context configuration."""
+    return long(seed, blocks_needed, num_seqs=1, ctx=131072, num_blocks=10240, device=device)
+
+
+# shapes measured beside the five configurations above (not among them)
+EXTRA_CONFIGS = {
+    "long1x131k_bf16": long_single,
+}
+
+
 def make(name: str, seed: int, blocks_needed: BlocksNeeded, device="cpu") -> Workload:
-    return FULL_CONFIGS[name](seed, blocks_needed, device=device)
+    fn = FULL_CONFIGS.get(name) or EXTRA_CONFIGS[name]
+    return fn(seed, blocks_needed, device=device)
