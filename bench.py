@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration measurements of all five workloads")
     ap.add_argument("--next-rows", action="store_true",
                     help="measure the NEXT rows instead (block fork / swap / pack, encode-only "
                          "attention, host block allocator): one JSON line each")
@@ -533,6 +535,194 @@ def run_e2e(args, w, w_out, step, stream, dev, flush_l2, use_graph):
                               "direct calls: copy-in, step, copy-out, L2 flushed before each step")
 
 
+def make_flush(dev):
+    """Writes 2x L2 of unrelated data, then reads another 2x L2, so that the
+    lines left in L2 are clean (no write-back of the flush lands in the next
+    timed step)."""
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)   # 258 MB, 2x L2
+    evict = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    evict_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        torch.sum(evict, dim=0, out=evict_sum)
+    return flush_l2
+
+
+def capture_graph(fn, dev, stream):
+    """fn(stream) run once, then captured as a CUDA graph on a side stream."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn(side)
+        side.synchronize()
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+            fn(side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    return g
+
+
+class StepRunner:
+    """One workload resident on the device, its step through the library's
+    one-call step entry points, and the timing of that step and of its main
+    attention kernel (CUDA events on the launching stream, L2 flushed before
+    each timed step)."""
+
+    def __init__(self, pa, w: W.Workload, dev, warmup: int, use_graph: bool):
+        self.pa, self.w, self.dev = pa, w, dev
+        self.decode_only = w.decode_only
+        self.max_q = int(w.q_lens.max())
+        self.slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(w.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws_bytes = (pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                             w.block_size, w.max_blocks) if self.decode_only else
+                    pa.varlen_prefill_workspace_size(w.num_seqs, w.total_q, w.num_heads, w.num_kv_heads,
+                                                     w.head_dim, w.block_size, w.max_blocks))
+        self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        # decode: plan (with the cache write), decode; mixed: plan (with the
+        # cache write and the prefill plan), decode, prefill
+        self.launches_per_step = 2 if self.decode_only else 3
+        for _ in range(max(warmup, 3)):
+            self.step()
+        torch.cuda.synchronize()
+        self.check_status("warm-up")
+        self.graph = capture_graph(lambda s: self.step(pa_stream=s), dev, self.stream) if use_graph else None
+        # the attention call alone, as a graph, for timing it on the device (a
+        # mixed call chains its kernels, so events around eager launches would
+        # also count host set-up between them)
+        self.attn_graph = None
+        if use_graph and not self.decode_only:
+            self.attn_graph = capture_graph(self.attention, dev, self.stream)
+
+    def step(self, q=None, key=None, value=None, bt=None, ctx=None, ss=None, cu=None, o=None,
+             pa_stream=None):
+        w, pa = self.w, self.pa
+        q = w.q if q is None else q
+        key = w.key if key is None else key
+        value = w.value if value is None else value
+        bt = w.block_tables if bt is None else bt
+        ctx = w.context_lens if ctx is None else ctx
+        ss = w.seq_start if ss is None else ss
+        cu = w.cu_seqlens_q if cu is None else cu
+        o = self.out if o is None else o
+        pa_stream = self.stream if pa_stream is None else pa_stream
+        if self.decode_only:
+            # slot mapping + cache write + decode through the one-call step entry
+            pa.decode_step(q, key, value, w.k_cache, w.v_cache, bt, ctx, ss, cu, w.scale, out=o,
+                           slot_mapping=self.slots, workspace=self.workspace, dev_status=self.status,
+                           stream=pa_stream)
+            return
+        # slot mapping + cache write + varlen attention through the one-call step entry
+        pa.varlen_step(q, key, value, w.k_cache, w.v_cache, cu, bt, ctx, ss, w.scale, self.max_q, out=o,
+                       slot_mapping=self.slots, workspace=self.workspace, dev_status=self.status,
+                       stream=pa_stream)
+
+    def attention(self, pa_stream):
+        w = self.w
+        self.pa.varlen_prefill(w.q, w.cu_seqlens_q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                               w.scale, self.max_q, out=self.out, workspace=self.workspace,
+                               dev_status=self.status, stream=pa_stream)
+
+    def check_status(self, when):
+        st = self.pa.get_device_status(self.status)
+        if st != 0:
+            raise RuntimeError(f"device status {self.pa.status_string(st)} {when} ({self.w.name})")
+
+    def time_steps(self, K: int, flush_l2):
+        """Device time of K steps, one by one (ms each)."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush_l2()
+            ev[i][0].record(self.stream)
+            if self.graph is not None:
+                self.graph.replay()
+            else:
+                self.step()
+            ev[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def time_kernel(self, n: int, flush_l2):
+        """Device time of the main attention kernel (ms each): the events the
+        library records around that launch on the launching stream (direct
+        launches); a mixed batch's attention call is timed as a graph of it."""
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in kev:
+            a.record(); b.record()
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush_l2()
+            if self.attn_graph is not None:
+                kev[i][0].record(self.stream)
+                self.attn_graph.replay()
+                kev[i][1].record(self.stream)
+            else:
+                self.pa.set_timing_events(*kev[i])
+                self.step()
+        self.pa.set_timing_events(None, None)
+        torch.cuda.synchronize()
+        self.check_status("in the timed region")
+        return [a.elapsed_time(b) for a, b in kev]
+
+
+def stats_us(ms):
+    return {"median": round(1e3 * float(np.median(ms)), 3), "mean": round(1e3 * float(np.mean(ms)), 3)}
+
+
+def measure_configs(args, pa, dev, flush_l2, n):
+    """Each of the five workload configurations through the same step and
+    timing as the headline: median and mean of n event-timed steps (L2 flushed
+    before each), its main attention kernel likewise, and its roofline
+    fraction.  For the mixed step also the prefill chunks alone."""
+    peak, _ = measured_peaks()
+    tc_peak = measured_tflops()
+    out = {}
+    for name in W.FULL_CONFIGS:
+        w = W.make(name, args.seed, pa.num_blocks_needed, device=dev)
+        r = StepRunner(pa, w, dev, 3, not args.no_graph)
+        step_ms = r.time_steps(n, flush_l2)
+        kern_ms = r.time_kernel(n, flush_l2)
+        r.check_status("in a config's timed region")
+        b = workload_bytes(w)
+        step_bytes = b["kv_unique"] + b["q"] + b["out"] + b["new_kv"] + b["meta"]
+        kern_bytes = b["kv_unique"] + b["q"] + b["out"]
+        km = float(np.median(kern_ms))
+        e = {"steps": n, "step_us": stats_us(step_ms), "kernel_us": stats_us(kern_ms),
+             "step_gbs": round(step_bytes / (float(np.median(step_ms)) / 1e3) / 1e9, 1)}
+        if w.decode_only:
+            e["kernel"] = "split_decode_kernel" if w.dtype == torch.bfloat16 else "generic_attention_kernel"
+            e["kernel_gbs"] = round(kern_bytes / (km / 1e3) / 1e9, 1)
+            e["frac"] = round(kern_bytes / (km / 1e3) / 1e9 / peak, 4)
+        else:
+            flops = prefill_flops(w)
+            e["kernel"] = "attention call: split_decode_kernel + prefill_kernel, concurrent"
+            e["decode_rows_gbs"] = round(kern_bytes / (km / 1e3) / 1e9, 1)
+            e["decode_rows_frac"] = round(kern_bytes / (km / 1e3) / 1e9 / peak, 4)
+            e["prefill_tflops"] = round(flops / (km / 1e3) / 1e12, 1)
+            e["prefill_frac_of_call"] = round(flops / (km / 1e3) / 1e12 / tc_peak, 4)
+        del r
+        if not w.decode_only:
+            # the step's prefill chunks alone (same prefixes, no decode rows): the
+            # call is a plan launch and the prefill kernel
+            wp = W.mixed(args.seed, pa.num_blocks_needed, num_decode=0, device=dev)
+            rp = StepRunner(pa, wp, dev, 3, not args.no_graph)
+            pm = rp.time_kernel(n, flush_l2)
+            pf = prefill_flops(wp)
+            pmed = float(np.median(pm))
+            e["prefill_alone"] = {"call_us": stats_us(pm), "flops": pf,
+                                  "tflops": round(pf / (pmed / 1e3) / 1e12, 1),
+                                  "frac": round(pf / (pmed / 1e3) / 1e12 / tc_peak, 4)}
+            del rp, wp
+        out[name] = e
+        del w
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     from pagedattention_kv_cache_reshape_gb300 import build, pa
     torch.cuda.set_device(local)
@@ -540,140 +730,35 @@ def run_ours(args, world, rank, local):
     build.build()
     pa.load()
     w = W.make(args.config, args.seed + rank, pa.num_blocks_needed, device=dev)
-    decode_only = w.decode_only
-    max_q = int(w.q_lens.max())
-    slots = torch.empty(w.total_q, dtype=torch.int64, device=dev)
-    out = torch.empty_like(w.q)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws_bytes = (pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
-                                         w.block_size, w.max_blocks) if decode_only else
-                pa.varlen_prefill_workspace_size(w.num_seqs, w.total_q, w.num_heads, w.num_kv_heads,
-                                                 w.head_dim, w.block_size, w.max_blocks))
-    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(q=w.q, key=w.key, value=w.value, bt=w.block_tables, ctx=w.context_lens,
-             ss=w.seq_start, cu=w.cu_seqlens_q, o=out, pa_stream=None):
-        pa_stream = stream if pa_stream is None else pa_stream
-        if decode_only:
-            # slot mapping + cache write + decode through the one-call step entry
-            pa.decode_step(q, key, value, w.k_cache, w.v_cache, bt, ctx, ss, cu, w.scale, out=o,
-                           slot_mapping=slots, workspace=workspace, dev_status=status, stream=pa_stream)
-            return
-        # slot mapping + cache write + varlen attention through the one-call step entry
-        pa.varlen_step(q, key, value, w.k_cache, w.v_cache, cu, bt, ctx, ss, w.scale, max_q, out=o,
-                       slot_mapping=slots, workspace=workspace, dev_status=status, stream=pa_stream)
-
-    # decode: plan (with the cache write), decode; mixed: plan (with the cache
-    # write and the prefill plan), decode, prefill
-    launches_per_step = 2 if decode_only else 3
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    st = pa.get_device_status(status)
-    if st != 0:
-        raise RuntimeError(f"device status {pa.status_string(st)} during warm-up")
-
-    graph = None
-    if not args.no_graph:
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            step(pa_stream=side)
-            side.synchronize()
-            with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
-                step(pa_stream=side)
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
-        graph = g
-
-    # the attention call alone, as a graph, for timing it on the device: the
-    # mixed call runs its decode rows and prefill chunks on two streams, so
-    # events around eager launches would also count host set-up between them
-    attn_graph = None
-    if not args.no_graph and not decode_only:
-        ga = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(ga, stream=side, capture_error_mode="thread_local"):
-                pa.varlen_prefill(w.q, w.cu_seqlens_q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
-                                  w.scale, max_q, out=out, workspace=workspace, dev_status=status,
-                                  stream=side)
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
-        attn_graph = ga
-
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)   # 258 MB, 2x L2
-    evict = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    evict.zero_()
-    evict_sum = torch.empty((), dtype=torch.float32, device=dev)
-
-    def flush_l2():
-        # write 2x L2 of unrelated data, then read another 2x L2 so the lines
-        # left in L2 are clean (no write-back of the flush inside the timed step)
-        flush.zero_()
-        torch.sum(evict, dim=0, out=evict_sum)
+    flush_l2 = make_flush(dev)
+    r = StepRunner(pa, w, dev, args.warmup, not args.no_graph)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for a, b in kev:
-        a.record(); b.record()
-    torch.cuda.synchronize()
 
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        for i in range(K):
-            flush_l2()
-            if graph is not None:
-                ev[i][0].record(stream)
-                graph.replay()
-                ev[i][1].record(stream)
-            else:
-                pa.set_timing_events(*kev[i])
-                ev[i][0].record(stream)
-                step()
-                ev[i][1].record(stream)
-        torch.cuda.synchronize()
+        step_ms = r.time_steps(K, flush_l2)
         t_wall = time.perf_counter() - t_wall0
-    pa.set_timing_events(None, None)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = float(sum(step_ms))
-
-    # dominant kernel on its own: the main attention kernel, timed by events the
-    # library records around that launch on the launching stream (direct
-    # launches); a mixed batch's attention call is timed as a graph of that call
-    kern_ms = []
-    for i in range(min(K, 100)):
-        flush_l2()
-        if attn_graph is not None:
-            kev[i][0].record(stream)
-            attn_graph.replay()
-            kev[i][1].record(stream)
-        else:
-            pa.set_timing_events(*kev[i])
-            step()
-    pa.set_timing_events(None, None)
-    torch.cuda.synchronize()
-    kern_ms = [a.elapsed_time(b) for a, b in kev[:min(K, 100)]]
-    st = pa.get_device_status(status)
-    if st != 0:
-        raise RuntimeError(f"device status {pa.status_string(st)} in the timed region")
+    kern_ms = r.time_kernel(min(K, 100), flush_l2)
 
     # end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, out, step, stream, dev, flush_l2, graph is not None)
+        e2e = run_e2e(args, w, r.out, r.step, r.stream, dev, flush_l2, r.graph is not None)
+
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = measure_configs(args, pa, dev, flush_l2, max(K, 50))
 
     return dict(w=w, total_ms=total_ms, step_ms=step_ms, kern_ms=kern_ms, clocks=clk.summary(),
-                graph=graph is not None, launches=launches_per_step * K, e2e=e2e, wall=t_wall)
+                graph=r.graph is not None, launches=r.launches_per_step * K, e2e=e2e, wall=t_wall,
+                configs=configs)
 
 
 def main():
@@ -715,6 +800,7 @@ def main():
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
+        "ms_per_step_median": round(float(np.median(r["step_ms"])), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -740,6 +826,8 @@ def main():
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
             "traffic": traffic, "bytes_per_launch": kern_bytes, "avg_launch_ms": round(kern_ms, 5),
+            "median_launch_ms": round(float(np.median(r["kern_ms"])), 5),
+            "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
         },
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
@@ -769,6 +857,10 @@ def main():
                        "frac": round(flops / call_s / 1e12 / tc_peak, 4),
                        "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops)"},
         })
+    if r["configs"] is not None:
+        # all five workloads, each timed like the headline (median of >= 50
+        # steps, L2 flushed before each); units: microseconds, GB/s, TFLOP/s
+        line["configs"] = r["configs"]
     if world == 1 and not args.no_cpu_baseline:
         import oracle as O
         nthreads = os.cpu_count() or 1

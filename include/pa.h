@@ -146,8 +146,9 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
  *     out[s][h] = sum_j softmax(x)_j V_s[j][g],
  * where K_s[j] = k_cache[block_tables[s][j / B]][j % B] (same for V).
  * context_lens counts the new token, which pa_reshape_and_cache has already
- * written.  Long contexts are split across thread blocks and merged by a
- * second kernel with the log-sum-exp rule
+ * written.  Long contexts are split across thread blocks; inside the same
+ * kernel, the warp that stores a sequence's last piece merges the pieces
+ * with the log-sum-exp rule
  *     M = max m_i,  L = sum l_i e^{m_i - M},  o = sum e^{m_i - M} o_i / L.
  *  out          device [num_seqs][num_heads][head_dim], dtype of q
  *  q            device [num_seqs][num_heads][head_dim]
@@ -174,10 +175,15 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const 
  *
  * The scratch is a fixed PA_STATIC_SCRATCH_BYTES (24 MiB) array inside the
  * library: every GPU that loads the library holds it until the process
- * exits.  A problem whose pa_decode_workspace_size(...) exceeds it returns
- * PA_ERR_WORKSPACE before anything is launched.  The call allocates nothing.
- * The first call on each device looks up the array's device address with a
- * synchronous CUDA runtime call, so make that first call before any stream
+ * exits.  Arguments are checked exactly as pa_decode checks them, with the
+ * same status codes.  Then, for a call that takes the split decode (bf16,
+ * head_dim 64/128, the shapes pa_decode serves with scratch), a problem whose
+ * pa_decode_workspace_size(...) exceeds the array returns PA_ERR_WORKSPACE
+ * before anything is launched; calls that take the CUDA-core kernel use no
+ * scratch and have no such limit.  The call allocates nothing.
+ * The first call on each device, and the first after a cudaDeviceReset
+ * (which makes a new CUDA context), looks up the array's device address with
+ * a synchronous CUDA runtime call, so make that call before any stream
  * capture.  Every call shares the one array and leaves its last contents
  * there; nothing in it has to start at zero.  Calls that can overlap on the
  * GPU (different streams, or several devices' threads targeting one device)
@@ -414,6 +420,42 @@ PA_API pa_status pa_reset_device_status(int32_t *dev_status, pa_stream_t stream)
  * NULL, NULL to stop.  The events are not owned by the library.
  */
 PA_API pa_status pa_set_timing_events(void *ev_begin, void *ev_end);
+
+/*
+ * Test hook for the bounded in-kernel waits (no counterpart on the pages).
+ * Every wait inside the library's pipelined kernels gives up after a time
+ * limit, records PA_ERR_TIMEOUT in *dev_status and lets its kernel return, so
+ * a stuck pipeline never hangs the GPU.  This hook lets a test reach those
+ * branches on purpose, without any fault: for every later pa_decode,
+ * pa_decode_step, pa_varlen_prefill, pa_varlen_step and pa_varlen_encode call
+ * made from the same host thread,
+ *  limit_ns  bounds each wait (0: the default of one second);
+ *  stall     makes one role of each CTA stop early and never give the signal
+ *            the others wait for (nobody ever sets it, so their waits run out):
+ *    PA_STALL_NONE      normal operation;
+ *    PA_STALL_PRODUCER  the CTA's copy producer issues `after` copies (decode:
+ *                       `after` blocks; prefill: `after` K/V tiles of keys or
+ *                       values) and then stops, so the consumers wait for
+ *                       data that never comes;
+ *    PA_STALL_CONSUMER  the CTA's consumers (decode: the attention warps, after
+ *                       `after` blocks; prefill: the MMA issuer, after `after`
+ *                       K/V tiles) stop, so the producer waits for ring slots
+ *                       that are never freed;
+ *  sites     (device int32, nullable) receives, OR-ed, one PA_WAIT_* bit per
+ *            role whose wait ran out (a role that stopped on purpose sets none).
+ * A CTA's own copies in flight are always waited for (one-second limit)
+ * before it exits.  The hook changes results only in that the stalled calls
+ * time out; PA_STALL_NONE with limit 0 restores normal operation.  Returns
+ * PA_ERR_INVALID_ARG for an unknown mode or a negative `after`.
+ */
+enum {
+    PA_STALL_NONE = 0, PA_STALL_PRODUCER = 1, PA_STALL_CONSUMER = 2
+};
+enum {
+    PA_WAIT_DECODE_PRODUCER = 1, PA_WAIT_DECODE_CONSUMER = 2, PA_WAIT_PREFILL_PRODUCER = 4,
+    PA_WAIT_PREFILL_MMA = 8, PA_WAIT_PREFILL_SOFTMAX = 16
+};
+PA_API pa_status pa_set_wait_test(uint64_t limit_ns, int stall, int after, int32_t *sites);
 
 #ifdef __cplusplus
 }

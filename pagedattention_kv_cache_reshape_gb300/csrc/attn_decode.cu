@@ -110,6 +110,11 @@ struct DecodeParams {
     int num_blocks;
     int num_kv_heads;
     const uint8_t *k_bytes, *v_bytes;   // the pools
+    // bounded waits: their limit, and the test hook's stall (PA_STALL_*)
+    uint64_t wait_ns;
+    int stall;
+    int stall_after;
+    int32_t *wait_sites;
 };
 
 // Optional cache write folded into the plan kernel (pa_decode_step): for new
@@ -684,8 +689,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                 if (lane == 0) {
                     const int k = issued;
                     const int stage = k % NS;
-                    if (k >= NS && !mbar_wait(empty + stage, ((k / NS) - 1) & 1)) {
+                    if (p.stall == PA_STALL_PRODUCER && k >= p.stall_after) {
+                        ok = false;   // test hook: stage k and later are never filled
+                    } else if (k >= NS && !mbar_wait(empty + stage, ((k / NS) - 1) & 1, p.wait_ns)) {
                         set_status(p.status, PA_ERR_TIMEOUT);
+                        note_wait_site(p.wait_sites, PA_WAIT_DECODE_PRODUCER);
                         abort_flag = 1;
                         ok = false;
                     }
@@ -730,7 +738,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
             cur = nxt;
             cur_hg = nxt_hg;
         }
-        // wait (bounded) until every copy this CTA issued has landed
+        // wait (bounded, always at the default limit) until every copy this CTA
+        // issued has landed
         if (lane == 0) {
             const int first_k = issued > NS ? issued - NS : 0;
             for (int k = first_k; k < issued; ++k) mbar_wait(full + (k % NS), (k / NS) & 1);
@@ -776,8 +785,13 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         for (bool first_block = true;; first_block = false) {
             const int stage = k % NS;
             if (*reinterpret_cast<volatile int *>(&abort_flag)) { aborted = true; break; }
-            if (!mbar_wait(full + stage, (k / NS) & 1)) {
-                if (lane == 0) set_status(p.status, PA_ERR_TIMEOUT);
+            // test hook: stop without releasing stage k, so the producer's wait runs out
+            if (p.stall == PA_STALL_CONSUMER && k >= p.stall_after) { aborted = true; break; }
+            if (!mbar_wait(full + stage, (k / NS) & 1, p.wait_ns)) {
+                if (lane == 0) {
+                    set_status(p.status, PA_ERR_TIMEOUT);
+                    note_wait_site(p.wait_sites, PA_WAIT_DECODE_CONSUMER);
+                }
                 abort_flag = 1;
                 aborted = true;
                 break;
@@ -1107,6 +1121,11 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.num_kv_heads = a.num_kv_heads;
     prm.k_bytes = static_cast<const uint8_t *>(a.k_cache);
     prm.v_bytes = static_cast<const uint8_t *>(a.v_cache);
+    const WaitTest &wt = wait_test();
+    prm.wait_ns = wt.limit_ns;
+    prm.stall = wt.stall;
+    prm.stall_after = wt.after;
+    prm.wait_sites = wt.sites;
 
     // tensor maps: one TMA per block for all kv-heads of the CTA
     CUtensorMap mk, mv;

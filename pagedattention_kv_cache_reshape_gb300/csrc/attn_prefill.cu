@@ -83,6 +83,11 @@ struct PrefillParams {
     // no wait at the start; the wait for the decode grid comes at the end, so
     // this grid completes after it and later work may rely on both.
     int wait_at_end;
+    // bounded waits: their limit, and the test hook's stall (PA_STALL_*)
+    uint64_t wait_ns;
+    int stall;
+    int stall_after;
+    int32_t *wait_sites;
 };
 
 static_assert(BN == kPrefillKeysPerTile, "the plan counts KV tiles of the main kernel's width");
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto phase_of = [](int n) { return (uint32_t)((n / kSlots) & 1); };
     // consumers: item `it` as the producer decoded it, with the read acknowledged
     auto take_item = [&](int it, Item &I) -> bool {
-        if (!mbar_wait(item_full + it % kItemSlots, (uint32_t)((it / kItemSlots) & 1))) return false;
+        if (!mbar_wait(item_full + it % kItemSlots, (uint32_t)((it / kItemSlots) & 1), p.wait_ns)) return false;
         I = items[it % kItemSlots];
         __syncwarp();
         if (lane == 0) mbar_arrive(item_empty + it % kItemSlots);
@@ -243,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSide));
     if (warp == kProducerWarp) {
         // ================= TMA producer
-        bool ok = true;
-        int n = 0, nq = 0;
+        bool ok = true, stopped = false;
+        int n = 0, nq = 0, issued_end = 0;   // issued_end: ring entries issued so far
         // item `it`: the next id from the counter (every item, the first one too:
         // CTAs that become resident late, behind a concurrent decode kernel,
         // must not hold on to long items); decoded once here and published one
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int w = total;
             if (lane == 0) {
                 if (it >= kItemSlots &&
-                    !mbar_wait(item_empty + it % kItemSlots, (uint32_t)(((it / kItemSlots) - 1) & 1)))
+                    !mbar_wait(item_empty + it % kItemSlots, (uint32_t)(((it / kItemSlots) - 1) & 1), p.wait_ns))
                     okp = false;
                 else
                     w = atomicAdd(p.next_item, 1);
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Q: its buffer is free once every QK product of the previous item completed
             if (lane == 0) {
-                if (nq >= 1 && !mbar_wait(q_empty, (uint32_t)((nq - 1) & 1))) ok = false;
+                if (nq >= 1 && !mbar_wait(q_empty, (uint32_t)((nq - 1) & 1), p.wait_ns)) ok = false;
                 if (ok) {
                     mbar_arrive_expect_tx(q_full, kMT * kQBytes);
                     for (int t = 0; t < kMT; ++t)
@@ -320,7 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int cb = __shfl_sync(kFull, ids_cur, ((j * kBlocksPerTile) & 31) + (b & (kBlocksPerTile - 1)));
                 for (int kv = 0; kv < 2; ++kv) {
                     const int m = n + 2 * j + kv;
-                    if (lane == 0 && m >= kSlots && !mbar_wait(kv_empty + slot_of(m), phase_of(m) ^ 1u)) ok = false;
+                    if (p.stall == PA_STALL_PRODUCER && m >= p.stall_after) {
+                        stopped = true;   // test hook: entry m and later are never filled
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0 && m >= kSlots && !mbar_wait(kv_empty + slot_of(m), phase_of(m) ^ 1u, p.wait_ns))
+                        ok = false;
                     ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
                     if (lane == 0) mbar_arrive_expect_tx(kv_full + slot_of(m), kSlotBytes);
@@ -328,15 +339,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane < kBlocksPerTile * kDH)
                         tma_load_5d(kv_s + slot_of(m) * kSlotBytes + dh * kPlaneKV + b * (kB * 128),
                                     kv ? &tmap_v : &tmap_k, 0, 0, dh, I.g, cb, kv_full + slot_of(m));
+                    issued_end = m + 1;
                 }
             }
             n += 2 * I.nkv;
         }
-        if (!ok && lane == 0) set_status(p.status, PA_ERR_TIMEOUT);
-        // every copy this CTA issued has landed before the CTA may exit
+        if (!ok && !stopped && lane == 0) {
+            set_status(p.status, PA_ERR_TIMEOUT);
+            note_wait_site(p.wait_sites, PA_WAIT_PREFILL_PRODUCER);
+        }
+        // every copy this CTA issued has landed before the CTA may exit (these
+        // waits keep the default limit whatever the test hook sets): the last Q,
+        // and the last kSlots ring entries issued (earlier ones were consumed)
         if (lane == 0) {
             if (nq >= 1) mbar_wait(q_full, (uint32_t)((nq - 1) & 1));
-            for (int m = n > kSlots ? n - kSlots : 0; m < n; ++m) mbar_wait(kv_full + slot_of(m), phase_of(m));
+            for (int m = issued_end > kSlots ? issued_end - kSlots : 0; m < issued_end; ++m)
+                mbar_wait(kv_full + slot_of(m), phase_of(m));
         }
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer: the whole warp follows the schedule,
@@ -379,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto commit = [&](uint64_t *bar) {
             if (leader) umma_commit(bar);
         };
-        bool ok = true;
+        bool ok = true, stopped = false;
         int n = 0, J = 0, nq = 0;
         for (int it = 0; ok; ++it) {
             Item I;
@@ -387,7 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!I.live) break;
             if (!I.valid) continue;
             const int nkv = __shfl_sync(kFull, I.nkv, 0);
-            if (!mbar_wait(q_full, (uint32_t)(nq & 1)) || !mbar_wait(kv_full + slot_of(n), phase_of(n))) {
+            if (p.stall == PA_STALL_CONSUMER && n >= p.stall_after) { stopped = true; ok = false; break; }
+            if (!mbar_wait(q_full, (uint32_t)(nq & 1), p.wait_ns) ||
+                !mbar_wait(kv_full + slot_of(n), phase_of(n), p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -401,13 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nkv; ++j) {
                 const bool next = j + 1 < nkv;
                 const int nv = n + 2 * j + 1, nk = n + 2 * j + 2;
-                if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv))) { ok = false; break; }
+                // test hook: stop, leaving ring entries unreleased, so the producer's wait runs out
+                if (p.stall == PA_STALL_CONSUMER && nv >= p.stall_after) { stopped = true; ok = false; break; }
+                if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
                 for (int t = 0; t < kMT; ++t) {
-                    if (!mbar_wait(p_full + t, (uint32_t)((J + j) & 1))) { ok = false; break; }
+                    if (!mbar_wait(p_full + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv(t, nv, j == 0);
                     if (next) {
-                        if (t == 0 && !mbar_wait(kv_full + slot_of(nk), phase_of(nk))) { ok = false; break; }
+                        if (t == 0 && !mbar_wait(kv_full + slot_of(nk), phase_of(nk), p.wait_ns)) { ok = false; break; }
                         tc_fence_after();
                         issue_qk(t, nk);
                         commit(s_full + t);
@@ -426,8 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             J += nkv;
             ++nq;
         }
-        if (!ok && leader) set_status(p.status, PA_ERR_TIMEOUT);
-        // drain: everything issued must finish before TMEM is released
+        if (!ok && !stopped && leader) {
+            set_status(p.status, PA_ERR_TIMEOUT);
+            note_wait_site(p.wait_sites, PA_WAIT_PREFILL_MMA);
+        }
+        // drain (default limit): everything issued must finish before TMEM is released
         commit(drained);
         mbar_wait(drained, 0);
         __syncwarp();
@@ -456,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lb_last = (I.ctx - 1) / kB;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < I.nkv; ++j) {
-                if (!mbar_wait(s_full + t, (uint32_t)((J + j) & 1))) { ok = false; break; }
+                if (!mbar_wait(s_full + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const int key0 = j * BN;
                 const bool diag = key0 + BN - 1 > first_pos;    // a key past some row of this tile
@@ -537,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int bb = lb_last - j * kBlocksPerTile;
                     if (bb >= 0 && bb < kBlocksPerTile) {
                         const int nv = n + 2 * j + 1;
-                        if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv))) { ok = false; break; }
+                        if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
                         uint8_t *vs = kv_s + slot_of(nv) * kSlotBytes;
                         const int rows_zero = kB - t_tail;
                         const int n16 = kDH * rows_zero * 8;
@@ -559,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- epilogue: O / l -> bf16 rows of out, after the last product into O_t.
             // The next item's first product into O_t waits for this warpgroup's
             // next P, so these TMEM loads complete before O_t is overwritten.
-            if (!mbar_wait(o_full + t, (uint32_t)(no & 1))) { ok = false; break; }
+            if (!mbar_wait(o_full + t, (uint32_t)(no & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             const float inv = 1.f / l;
             __nv_bfloat16 *dst = p.out + ((int64_t)(I.q0 + I.i0 + i) * p.num_heads +
@@ -586,7 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             J += I.nkv;
             ++no;
         }
-        if (!ok && r == 0) set_status(p.status, PA_ERR_TIMEOUT);
+        if (!ok && r == 0) {
+            set_status(p.status, PA_ERR_TIMEOUT);
+            note_wait_site(p.wait_sites, PA_WAIT_PREFILL_SOFTMAX);
+        }
     }
 
     tc_fence_before();
@@ -728,6 +756,11 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     prm.status = a.status;
     prm.causal = a.causal;
     prm.wait_at_end = planned ? 1 : 0;
+    const WaitTest &wt = wait_test();
+    prm.wait_ns = wt.limit_ns;
+    prm.stall = wt.stall;
+    prm.stall_after = wt.after;
+    prm.wait_sites = wt.sites;
     // persistent: one CTA per SM, never more CTAs than work items
     const size_t items = (size_t)job.capacity * (size_t)a.num_kv_heads;
     const int sms = device_sm_count();

@@ -29,8 +29,11 @@ int device_sm_count() {
 
 namespace {
 thread_local cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+thread_local WaitTest g_wait_test;
 
 }  // namespace
+
+const WaitTest &wait_test() { return g_wait_test; }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -85,6 +88,29 @@ pa_status check_attention_shape(int num_seqs, int num_heads, int num_kv_heads, i
 }
 
 }  // namespace
+
+pa_status decode_requirements(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks, int num_blocks, float scale, pa_dtype dtype, size_t *need) {
+    *need = 0;
+    pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                         max_blocks, num_blocks, dtype, scale);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    const int eb = elem_bytes(dtype);
+    if (!aligned(out, eb) || !aligned(q, eb) || !aligned(k_cache, eb) || !aligned(v_cache, eb))
+        return PA_ERR_INVALID_ARG;
+    AttnArgs a{const_cast<void *>(out), q, k_cache, v_cache, block_tables, context_lens, nullptr,
+               num_seqs, num_seqs, 1, num_heads, num_kv_heads, head_dim, block_size,
+               max_blocks, num_blocks, scale, dtype, nullptr};
+    if (split_decode_supported(a))
+        *need = split_decode_workspace(num_seqs, num_heads, head_dim, max_blocks);
+    return PA_OK;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -166,22 +192,17 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
                     int max_blocks, int num_blocks, float scale, pa_dtype dtype,
                     void *workspace, size_t workspace_bytes, int32_t *dev_status,
                     pa_stream_t stream) {
-    pa_status st = check_attention_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                                         max_blocks, num_blocks, dtype, scale);
+    size_t need = 0;
+    const pa_status st = decode_requirements(out, q, k_cache, v_cache, block_tables, context_lens,
+                                             num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                             max_blocks, num_blocks, scale, dtype, &need);
     if (st != PA_OK) return st;
     if (num_seqs == 0) return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
-        return PA_ERR_INVALID_ARG;
-    const int eb = elem_bytes(dtype);
-    if (!aligned(out, eb) || !aligned(q, eb) || !aligned(k_cache, eb) || !aligned(v_cache, eb))
-        return PA_ERR_INVALID_ARG;
     AttnArgs a{out, q, k_cache, v_cache, block_tables, context_lens, nullptr,
                num_seqs, num_seqs, 1, num_heads, num_kv_heads, head_dim, block_size,
                max_blocks, num_blocks, scale, dtype, dev_status};
     cudaStream_t s = (cudaStream_t)stream;
-    if (split_decode_supported(a)) {
-        const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
-                                                     block_size, max_blocks);
+    if (need > 0) {
         if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
         return from_cuda(launch_split_decode(a, workspace, workspace_bytes, s, true));
     }
@@ -423,6 +444,15 @@ pa_status pa_set_timing_events(void *ev_begin, void *ev_end) {
     if ((ev_begin == nullptr) != (ev_end == nullptr)) return PA_ERR_INVALID_ARG;
     g_ev_begin = static_cast<cudaEvent_t>(ev_begin);
     g_ev_end = static_cast<cudaEvent_t>(ev_end);
+    return PA_OK;
+}
+
+pa_status pa_set_wait_test(uint64_t limit_ns, int stall, int after, int32_t *sites) {
+    if (stall < PA_STALL_NONE || stall > PA_STALL_CONSUMER || after < 0) return PA_ERR_INVALID_ARG;
+    g_wait_test.limit_ns = limit_ns == 0 ? kWaitLimitNs : limit_ns;
+    g_wait_test.stall = stall;
+    g_wait_test.after = after;
+    g_wait_test.sites = sites;
     return PA_OK;
 }
 

@@ -16,6 +16,11 @@ __device__ __forceinline__ void set_status(int32_t *status, int32_t code) {
     if (status) atomicCAS(reinterpret_cast<int *>(status), 0, code);
 }
 
+// Records which role's bounded wait ran out (test hook; null: not recorded).
+__device__ __forceinline__ void note_wait_site(int32_t *sites, int32_t bit) {
+    if (sites) atomicOr(reinterpret_cast<int *>(sites), bit);
+}
+
 __device__ __forceinline__ float to_float(float x) { return x; }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <typename T> __device__ __forceinline__ T from_float(float x);

@@ -53,6 +53,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 void timing_begin(cudaStream_t stream);
 void timing_end(cudaStream_t stream);
 
+// Bounded-wait test settings (pa_set_wait_test) of the calling host thread,
+// passed to the pipelined kernels as launch parameters.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // default limit of an in-kernel wait
+struct WaitTest {
+    uint64_t limit_ns = kWaitLimitNs;
+    int stall = PA_STALL_NONE;
+    int after = 0;
+    int32_t *sites = nullptr;
+};
+const WaitTest &wait_test();
+
 cudaError_t launch_slot_mapping(const int32_t *block_tables, int num_seqs, int max_blocks,
                                 const int32_t *seq_start, const int32_t *cu_seqlens_q,
                                 int total_new, int block_size, int num_blocks,
@@ -75,6 +86,15 @@ cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k
 // row and kv-head).  row_filter selects the sequences it computes.
 constexpr int kAllRows = 0, kSkipSingleRows = 1, kOnlySingleRows = 2;
 cudaError_t launch_generic_attention(const AttnArgs &a, int row_filter, cudaStream_t stream);
+
+// pa_decode's host-side argument checks, in pa_decode's order and with its
+// status codes.  On PA_OK, *need is the workspace the call takes: the split
+// decode's scratch, or 0 when it runs the CUDA-core kernel (no scratch) or
+// num_seqs is 0.
+pa_status decode_requirements(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks, int num_blocks, float scale, pa_dtype dtype, size_t *need);
 
 // Persistent TMA + tensor-core split-KV decode (bf16, head_dim 64/128).
 bool split_decode_supported(const AttnArgs &a);

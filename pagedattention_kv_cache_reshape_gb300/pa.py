@@ -29,9 +29,12 @@ EXPORTS = (
     "pa_copy_blocks", "pa_varlen_encode", "pa_varlen_step",
     "pa_block_manager_create", "pa_block_manager_destroy", "pa_block_manager_num_free",
     "pa_block_manager_refcount", "pa_allocate_slots", "pa_free_sequence", "pa_share_prefix",
-    "pa_block_manager_tables", "pa_validate_inputs", "pa_allocate_slots_batch",
+    "pa_block_manager_tables", "pa_validate_inputs", "pa_allocate_slots_batch", "pa_set_wait_test",
 )
 STATIC_SCRATCH_BYTES = 24 << 20
+STALL_NONE, STALL_PRODUCER, STALL_CONSUMER = 0, 1, 2
+WAIT_DECODE_PRODUCER, WAIT_DECODE_CONSUMER = 1, 2
+WAIT_PREFILL_PRODUCER, WAIT_PREFILL_MMA, WAIT_PREFILL_SOFTMAX = 4, 8, 16
 
 
 class PAError(RuntimeError):
@@ -100,6 +103,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.pa_reset_device_status.argtypes = [vp, vp]
         L.pa_set_timing_events.restype = i32
         L.pa_set_timing_events.argtypes = [vp, vp]
+        L.pa_set_wait_test.restype = i32
+        L.pa_set_wait_test.argtypes = [ctypes.c_uint64, i32, i32, vp]
         L.pa_copy_blocks.restype = i32
         L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp, i32, vp, vp]
         L.pa_decode_step.restype = i32
@@ -390,6 +395,15 @@ def set_timing_events(ev_begin=None, ev_end=None) -> None:
             ev.record()
         return ev.cuda_event
     _check(load().pa_set_timing_events(handle(ev_begin), handle(ev_end)), "pa_set_timing_events")
+
+
+def set_wait_test(limit_ns: int = 0, stall: int = STALL_NONE, after: int = 0, sites=None) -> None:
+    """pa_set_wait_test: the bounded in-kernel waits' limit (0 = one second) and
+    the test stall for later calls from this thread; sites is an optional
+    device int32 tensor that receives the WAIT_* bits of the waits that ran out."""
+    _check(load().pa_set_wait_test(int(limit_ns), int(stall), int(after),
+                                   None if sites is None else _dev(sites, "sites", torch.int32)),
+           "pa_set_wait_test")
 
 
 def decode_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale: float, out=None,

@@ -127,3 +127,13 @@ def test_missing_library_fails_loudly(tmp_path):
             mod.load(str(tmp_path / "nope.so"))
     finally:
         mod._lib = saved
+
+
+def test_wait_test_hook_checks_its_arguments(lib):
+    # host-only: an unknown stall mode or a negative count is rejected; valid
+    # settings are taken, and the defaults restore normal operation
+    assert lib.pa_set_wait_test(0, 3, 0, None) == pa.ERR_INVALID_ARG
+    assert lib.pa_set_wait_test(0, -1, 0, None) == pa.ERR_INVALID_ARG
+    assert lib.pa_set_wait_test(0, pa.STALL_PRODUCER, -2, None) == pa.ERR_INVALID_ARG
+    assert lib.pa_set_wait_test(5_000_000, pa.STALL_CONSUMER, 4, None) == pa.OK
+    assert lib.pa_set_wait_test(0, pa.STALL_NONE, 0, None) == pa.OK
