@@ -784,10 +784,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         bool aborted = false;
         for (bool first_block = true;; first_block = false) {
             const int stage = k % NS;
-            if (*reinterpret_cast<volatile int *>(&abort_flag)) { aborted = true; break; }
+            // (another warp may set the flag meanwhile: one answer for the whole warp)
+            if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int *>(&abort_flag) != 0)) { aborted = true; break; }
             // test hook: stop without releasing stage k, so the producer's wait runs out
             if (p.stall == PA_STALL_CONSUMER && k >= p.stall_after) { aborted = true; break; }
-            if (!mbar_wait(full + stage, (k / NS) & 1, p.wait_ns)) {
+            if (!mbar_wait_warp(full + stage, (k / NS) & 1, p.wait_ns)) {
                 if (lane == 0) {
                     set_status(p.status, PA_ERR_TIMEOUT);
                     note_wait_site(p.wait_sites, PA_WAIT_DECODE_CONSUMER);

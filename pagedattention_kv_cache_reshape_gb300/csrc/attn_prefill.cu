@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto phase_of = [](int n) { return (uint32_t)((n / kSlots) & 1); };
     // consumers: item `it` as the producer decoded it, with the read acknowledged
     auto take_item = [&](int it, Item &I) -> bool {
-        if (!mbar_wait(item_full + it % kItemSlots, (uint32_t)((it / kItemSlots) & 1), p.wait_ns)) return false;
+        if (!mbar_wait_warp(item_full + it % kItemSlots, (uint32_t)((it / kItemSlots) & 1), p.wait_ns)) return false;
         I = items[it % kItemSlots];
         __syncwarp();
         if (lane == 0) mbar_arrive(item_empty + it % kItemSlots);
@@ -357,14 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(kv_full + slot_of(m), phase_of(m));
         }
     } else if (warp == kMmaWarp) {
-        // ================= MMA issuer: the whole warp follows the schedule,
-        // lane 0 issues.  Tensor-pipe order, per KV tile j of an item:
+        // ================= MMA issuer: the whole warp follows the schedule and
+        // executes the MMA and commit wrappers; one elected lane issues them.  Tensor-pipe order, per KV tile j of an item:
         //   PV_0(j)  QK_0(j+1)  PV_1(j)  QK_1(j+1)
         // so the products of one M-tile run while the other tile's softmax
         // turns S into P.  QK_t(j+1) (or QK_t(0) of the next item) overwrites
         // the TMEM columns that PV_t(j) reads P_t from; the tensor pipe runs
         // one thread's MMAs in issue order, so the read precedes the overwrite.
-        const bool leader = lane == 0;
         const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(kv_s);
         // descriptors: constant fields + (address >> 4) in bits 0..13
         const uint64_t dq = umma_desc_sw128(q_addr, 16, 1024);
@@ -375,28 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // single issuing thread keep closer to the tensor pipe.
         auto issue_qk = [&](int t, int nk) {      // S_t = Q_t K^T, K in ring entry nk
             const uint32_t ko = (uint32_t)slot_of(nk) * kSlotBytes;
-            if (leader) {
 #pragma unroll
-                for (int pl = 0; pl < D / 64; ++pl)
-                    umma_bf16_k64(tmem + s_col(t), dq + ((uint32_t)(t * kQBytes + pl * kPlaneQ) >> 4),
-                                  dk + ((ko + pl * kPlaneKV) >> 4), kIdescQK, pl > 0 ? 1u : 0u);
-            }
-            __syncwarp();
+            for (int pl = 0; pl < D / 64; ++pl)
+                umma_bf16_k64(tmem + s_col(t), dq + ((uint32_t)(t * kQBytes + pl * kPlaneQ) >> 4),
+                              dk + ((ko + pl * kPlaneKV) >> 4), kIdescQK, pl > 0 ? 1u : 0u);
         };
         auto issue_pv = [&](int t, int nv, bool first) {   // O_t (+)= P_t V, V in ring entry nv
             const uint32_t vo = (uint32_t)slot_of(nv) * kSlotBytes;
-            if (leader) {
 #pragma unroll
-                for (int kq = 0; kq < BN / 64; ++kq)   // 64 keys (4 MMAs of 16) per block
-                    umma_bf16_tmem_a_k64(tmem + o_col(t), tmem + s_col(t) + kq * 32,
-                                         dv + ((vo + kq * 4 * 2048) >> 4), kIdescPV, 2048 >> 4,
-                                         (!first || kq > 0) ? 1u : 0u);
-            }
-            __syncwarp();
+            for (int kq = 0; kq < BN / 64; ++kq)   // 64 keys (4 MMAs of 16) per block
+                umma_bf16_tmem_a_k64(tmem + o_col(t), tmem + s_col(t) + kq * 32,
+                                     dv + ((vo + kq * 4 * 2048) >> 4), kIdescPV, 2048 >> 4,
+                                     (!first || kq > 0) ? 1u : 0u);
         };
-        auto commit = [&](uint64_t *bar) {
-            if (leader) umma_commit(bar);
-        };
+        auto commit = [&](uint64_t *bar) { umma_commit(bar); };
         bool ok = true, stopped = false;
         int n = 0, J = 0, nq = 0;
         for (int it = 0; ok; ++it) {
@@ -406,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!I.valid) continue;
             const int nkv = __shfl_sync(kFull, I.nkv, 0);
             if (p.stall == PA_STALL_CONSUMER && n >= p.stall_after) { stopped = true; ok = false; break; }
-            if (!mbar_wait(q_full, (uint32_t)(nq & 1), p.wait_ns) ||
-                !mbar_wait(kv_full + slot_of(n), phase_of(n), p.wait_ns)) {
+            if (!mbar_wait_warp(q_full, (uint32_t)(nq & 1), p.wait_ns) ||
+                !mbar_wait_warp(kv_full + slot_of(n), phase_of(n), p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -423,13 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nv = n + 2 * j + 1, nk = n + 2 * j + 2;
                 // test hook: stop, leaving ring entries unreleased, so the producer's wait runs out
                 if (p.stall == PA_STALL_CONSUMER && nv >= p.stall_after) { stopped = true; ok = false; break; }
-                if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
+                if (!mbar_wait_warp(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
                 for (int t = 0; t < kMT; ++t) {
-                    if (!mbar_wait(p_full + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
+                    if (!mbar_wait_warp(p_full + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv(t, nv, j == 0);
                     if (next) {
-                        if (t == 0 && !mbar_wait(kv_full + slot_of(nk), phase_of(nk), p.wait_ns)) { ok = false; break; }
+                        if (t == 0 && !mbar_wait_warp(kv_full + slot_of(nk), phase_of(nk), p.wait_ns)) { ok = false; break; }
                         tc_fence_after();
                         issue_qk(t, nk);
                         commit(s_full + t);
@@ -448,13 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             J += nkv;
             ++nq;
         }
-        if (!ok && !stopped && leader) {
+        if (!ok && !stopped && lane == 0) {
             set_status(p.status, PA_ERR_TIMEOUT);
             note_wait_site(p.wait_sites, PA_WAIT_PREFILL_MMA);
         }
         // drain (default limit): everything issued must finish before TMEM is released
         commit(drained);
-        mbar_wait(drained, 0);
+        mbar_wait_warp(drained, 0);
         __syncwarp();
     }
     } else {
@@ -481,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lb_last = (I.ctx - 1) / kB;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < I.nkv; ++j) {
-                if (!mbar_wait(s_full + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
+                if (!mbar_wait_warp(s_full + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const int key0 = j * BN;
                 const bool diag = key0 + BN - 1 > first_pos;    // a key past some row of this tile
@@ -562,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int bb = lb_last - j * kBlocksPerTile;
                     if (bb >= 0 && bb < kBlocksPerTile) {
                         const int nv = n + 2 * j + 1;
-                        if (!mbar_wait(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
+                        if (!mbar_wait_warp(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
                         uint8_t *vs = kv_s + slot_of(nv) * kSlotBytes;
                         const int rows_zero = kB - t_tail;
                         const int n16 = kDH * rows_zero * 8;
@@ -584,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- epilogue: O / l -> bf16 rows of out, after the last product into O_t.
             // The next item's first product into O_t waits for this warpgroup's
             // next P, so these TMEM loads complete before O_t is overwritten.
-            if (!mbar_wait(o_full + t, (uint32_t)(no & 1), p.wait_ns)) { ok = false; break; }
+            if (!mbar_wait_warp(o_full + t, (uint32_t)(no & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             const float inv = 1.f / l;
             __nv_bfloat16 *dst = p.out + ((int64_t)(I.q0 + I.i0 + i) * p.num_heads +

@@ -130,6 +130,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Bounded wait of a converged warp whose outcome is the same in every lane:
+// false if any lane's wait ran out, so the warp never splits on a timeout
+// right at the limit (its next warp-wide instruction needs all 32 lanes).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
+                                               uint64_t limit_ns = 1000000000ull) {
+    const bool ok = mbar_wait(bar, parity, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA copies
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
@@ -214,24 +223,30 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int b_mn_ma
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The MMA and commit wrappers below are warp-collective: all 32 lanes of a
+// converged warp execute them, and `elect.sync` picks the one lane that
+// issues.  Issued this way a tcgen05.mma costs about 65 cycles of the warp's
+// time (GB300), against about 100 from inside a lane-0 branch; at M = N = 128
+// that is the tensor pipe's own 64 cycles per MMA, so any other instruction
+// of the issuing warp is a pipe bubble.
+
 // Four chained MMAs over K = 64 (one 128-byte swizzled plane of both
 // operands): step k reads A and B 32 bytes further along their rows (the
 // descriptors' address field, in 16-byte units, advances by 2).  The first
-// accumulates into D only if `accumulate`; the rest always do.  One asm block
-// keeps the issuing thread's instruction stream to the MMAs and two adds each.
+// accumulates into D only if `accumulate`; the rest always do.
 __device__ __forceinline__ void umma_bf16_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .b64 a, b;\n\t.reg .pred p0, p1;\n\t"
-        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+        "{\n\t.reg .b64 a, b;\n\t.reg .pred p0, e;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
         "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
         "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
         "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(1u));
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Four chained MMAs with the A operand read from tensor memory, over K = 64:
@@ -242,22 +257,24 @@ __device__ __forceinline__ void umma_bf16_k64(uint32_t d_tmem, uint64_t a_desc, 
 __device__ __forceinline__ void umma_bf16_tmem_a_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                      uint32_t idesc, uint32_t b_step, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .b64 b, bs;\n\t.reg .b32 a;\n\t.reg .pred p0, p1;\n\t"
-        "setp.ne.b32 p0, %5, 0;\n\tsetp.ne.b32 p1, %6, 0;\n\tcvt.u64.u32 bs, %4;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "{\n\t.reg .b64 b, bs;\n\t.reg .b32 a;\n\t.reg .pred p0, e;\n\t"
+        "setp.ne.b32 p0, %5, 0;\n\tcvt.u64.u32 bs, %4;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
         "add.s32 a, %1, 8;\n\tadd.s64 b, %2, bs;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
         "add.s32 a, a, 8;\n\tadd.s64 b, b, bs;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
         "add.s32 a, a, 8;\n\tadd.s64 b, b, bs;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(b_step), "r"(accumulate), "r"(1u));
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(b_step), "r"(accumulate));
 }
 
-// Arrives once on `bar` when every tcgen05 operation this thread issued so far completes.
+// Arrives once on `bar` when every tcgen05 operation the issuing lane issued
+// so far completes (warp-collective: one elected lane commits).
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
             smem_u32(bar))
         : "memory");
 }
