@@ -44,9 +44,11 @@
  *      key, value   [num_tokens][num_kv_heads][head_dim], token stride given
  *      slot_mapping int64 [num_tokens]
  *  - q-head h reads kv-head h / (num_heads / num_kv_heads) (MHA, GQA, MQA).
- *  - Supported: block_size 16; head_dim 64 or 128; pa_dtype F32 or BF16 for
- *    q, key/value, pools and out alike (fp32 accumulation in every case).
- *    Anything else returns PA_ERR_UNSUPPORTED.
+ *  - Supported: block_size 8, 16 or 32 for the attention calls (any block
+ *    size >= 1 for pa_compute_slot_mapping and pa_reshape_and_cache); head_dim
+ *    64 or 128; pa_dtype F32 or BF16 for q, key/value, pools and out alike
+ *    (fp32 accumulation in every case).  Anything else returns
+ *    PA_ERR_UNSUPPORTED.
  */
 #ifndef PA_H
 #define PA_H

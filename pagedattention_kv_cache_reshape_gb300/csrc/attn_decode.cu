@@ -48,7 +48,11 @@
 namespace pa {
 namespace {
 
-constexpr int kB = kBlockSize;  // 16 tokens per block
+// Block sizes (tokens per cache block) the fast decode takes: 8, 16 and 32.
+// A block is processed as max(1, B/16) sub-tiles of 16 tokens, the M of the
+// m16n8k16 products; at B = 8 the tile's upper 8 rows are masked like a
+// partly filled block's tail.
+constexpr int kSubTok = 16;
 constexpr int kMaxKvhPerCta = 8;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxQHeadsPerCta = 32;
@@ -165,9 +169,10 @@ __global__ void __launch_bounds__(kPlanThreads)
     decode_plan_kernel(const int32_t *__restrict__ context_lens,
                        const int32_t *__restrict__ cu_seqlens_q,
                        const int32_t *__restrict__ block_tables, int num_seqs, int max_blocks,
-                       int num_blocks, int total_q, int32_t *__restrict__ prefix,
+                       int num_blocks, int total_q, int log2b, int32_t *__restrict__ prefix,
                        StreamEntry *__restrict__ stream, int32_t *status, const KvWriteJob job,
                        const DecodeSplit split, const PrefillPlanJob prefill) {
+    const int B = 1 << log2b;   // tokens per cache block
     extern __shared__ __align__(16) int32_t pref_s[];  // [num_seqs + 1]
     __shared__ int32_t warp_tot[kPlanThreads / 32];
     __shared__ double pair_tot[kPlanThreads / 32];
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(kPlanThreads)
                     st = __ldg(job.seq_start + lo);
                 }
                 const int64_t pos = (int64_t)st + (t - c0);
-                const int64_t logical = pos / kB;
+                const int64_t logical = pos >> log2b;
                 // every chunk of the token finds the same slot; the first records it
                 if (pos < 0 || logical >= max_blocks) {
                     if (v0 == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(kPlanThreads)
                     if (phys < 0 || phys >= num_blocks) {
                         if (v0 == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
                     } else {
-                        slot = (int64_t)phys * kB + (pos - logical * kB);
+                        slot = ((int64_t)phys << log2b) + (pos - (logical << log2b));
                     }
                 }
                 if (v0 == 0) job.slot_mapping[t] = slot;
@@ -277,10 +282,10 @@ __global__ void __launch_bounds__(kPlanThreads)
             if (q0 < 0 || q1 < q0 || q1 > total_q) {
                 if (blockIdx.x == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
             } else if (q_len == 1) {
-                if (ctx <= 0 || (int64_t)ctx > (int64_t)max_blocks * kB) {
+                if (ctx <= 0 || (int64_t)ctx > (int64_t)max_blocks * B) {
                     if (blockIdx.x == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
                 } else {
-                    nb = (ctx + kB - 1) / kB;
+                    nb = (ctx + B - 1) >> log2b;
                 }
             }
         }
@@ -342,8 +347,8 @@ __global__ void __launch_bounds__(kPlanThreads)
             set_status(status, PA_ERR_OUT_OF_RANGE);
             blk = -1;
         }
-        const int ntok = min(kB, ctx - lb * kB);
-        const int seq_end = (lb + 1) * kB >= ctx ? 1 : 0;
+        const int ntok = min(B, ctx - lb * B);
+        const int seq_end = (lb + 1) * B >= ctx ? 1 : 0;
         StreamEntry e;
         e.seq = s;
         e.qrow = cu_seqlens_q ? __ldg(cu_seqlens_q + s) : s;
@@ -534,7 +539,7 @@ __device__ __forceinline__ void merge_group(const DecodeParams &p, int64_t slot0
 // consumer warps: the producer goes straight on to its wait and first
 // copies); they meet at named barrier 1.  warp_tot is shared memory for one
 // int per warp.
-template <int D>
+template <int D, int kB>
 __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int nblocks, int32_t *warp_tot,
                                                       int nthr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -606,12 +611,13 @@ __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int
 }
 
 // ------------------------------------------------------------------ main kernel
-template <int D>
+template <int D, int kB>
 __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     split_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
     constexpr int kHeadTileBytes = kB * D * 2;    // one kv-head of one block
     constexpr int kKSteps = D / 16;
+    constexpr int kSub = kB > kSubTok ? kB / kSubTok : 1;   // 16-token sub-tiles of a block
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -638,7 +644,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
-    if (p.context_lens && warp < cwarps) prefetch_first_blocks<D>(p, NS, pf_warp_tot, 32 * cwarps);
+    if (p.context_lens && warp < cwarps) prefetch_first_blocks<D, kB>(p, NS, pf_warp_tot, 32 * cwarps);
     grid_dependency_wait();      // the plan (and everything before it) is complete
     grid_dependents_launch();    // the next kernel may become resident
 
@@ -811,22 +817,37 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
             if (h.flags & kValid) {
                 const uint32_t kbase = smem_u32(st + kh * kHeadTileBytes);
                 const uint32_t vbase = smem_u32(st + kv_tile + kh * kHeadTileBytes);
-                // ---- S^T = K Q^T: A = K (tokens x 16 dims per step), B = Q^T
-                float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < kKSteps; ++ks) {
-                    const int chunk = ((ks & 3) << 1) + v_dsub;
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kbase + (ks >> 2) * (kB * 128) + v_tok * 128 + ((chunk ^ (v_tok & 7)) << 4),
-                            a0, a1, a2, a3);
-                    mma_bf16_16816(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-                }
-                // ---- online softmax per head column (heads 2q, 2q+1; tokens r, r+8)
                 const int ntok = h.ntok;
-                float x[4];
+                // sub-tiles past the valid tokens (a partly filled block of 32) are skipped
+                const int nsub = kSub == 1 ? 1 : (ntok + kSubTok - 1) / kSubTok;
+                // ---- S^T = K Q^T per 16-token sub-tile: A = K (tokens x 16 dims per step), B = Q^T
+                float x[kSub][4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = (r + (i >> 1) * 8) < ntok ? s4[i] * p.scale_log2 : -INFINITY;
-                float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+                for (int u = 0; u < kSub; ++u) {
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (u < nsub) {
+#pragma unroll
+                        for (int ks = 0; ks < kKSteps; ++ks) {
+                            const int chunk = ((ks & 3) << 1) + v_dsub;
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(kbase + (ks >> 2) * (kB * 128) + (u * kSubTok + v_tok) * 128 +
+                                        ((chunk ^ (v_tok & 7)) << 4),
+                                    a0, a1, a2, a3);
+                            mma_bf16_16816(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                        }
+                    }
+                    // tokens past ntok (the block's tail, or rows 8-15 of an 8-token block) are masked
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        x[u][i] = (u * kSubTok + r + (i >> 1) * 8) < ntok ? s4[i] * p.scale_log2 : -INFINITY;
+                }
+                // ---- online softmax per head column (heads 2q, 2q+1; tokens r, r+8 of each sub-tile)
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < kSub; ++u) {
+                    mx0 = fmax3(mx0, x[u][0], x[u][2]);
+                    mx1 = fmax3(mx1, x[u][1], x[u][3]);
+                }
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -835,10 +856,19 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                 // ntok >= 1, so every column has a finite max
                 const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
                 const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
-                const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
-                const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
-                l_part[0] = l_part[0] * al0 + (p0 + p2);
-                l_part[1] = l_part[1] * al1 + (p1 + p3);
+                float pr[kSub][4];
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int u = 0; u < kSub; ++u) {
+                    pr[u][0] = fast_exp2(x[u][0] - mn0);
+                    pr[u][1] = fast_exp2(x[u][1] - mn1);
+                    pr[u][2] = fast_exp2(x[u][2] - mn0);
+                    pr[u][3] = fast_exp2(x[u][3] - mn1);
+                    ls0 += pr[u][0] + pr[u][2];
+                    ls1 += pr[u][1] + pr[u][3];
+                }
+                l_part[0] = l_part[0] * al0 + ls0;
+                l_part[1] = l_part[1] * al1 + ls1;
                 m_run[0] = mn0;
                 m_run[1] = mn1;
 #pragma unroll
@@ -848,25 +878,31 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                     ot[j][2] *= al0;
                     ot[j][3] *= al1;
                 }
-                // P^T as the B operand: (token, head) pairs transposed to (head, token)
-                const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));   // tokens 0..7
-                const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));   // tokens 8..15
-                // masks for value rows past the sequence end (they may hold anything)
-                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                if (ntok < kB) {
-                    const int t0 = quad * 2;
-                    mlo = (t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u);
-                    mhi = (t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u);
-                }
-                // ---- O^T += V^T P^T: A = V^T (16 dims x 16 tokens per m-tile)
 #pragma unroll
-                for (int j = 0; j < kMTiles; ++j) {
-                    const int chunk = ((j & 3) << 1) + k_dsub;
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_t(vbase + (j >> 2) * (kB * 128) + k_tok * 128 + ((chunk ^ (k_tok & 7)) << 4),
-                              v0, v1, v2, v3);
-                    v0 &= mlo; v1 &= mlo; v2 &= mhi; v3 &= mhi;
-                    mma_bf16_16816(ot[j], v0, v1, v2, v3, pb0, pb1);
+                for (int u = 0; u < kSub; ++u) {
+                    if (u >= nsub) break;
+                    // P^T as the B operand: (token, head) pairs transposed to (head, token)
+                    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(pr[u][0], pr[u][1]));   // tokens 0..7
+                    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(pr[u][2], pr[u][3]));   // tokens 8..15
+                    // masks for value rows past the valid tokens (they may hold anything)
+                    const int nt = ntok - u * kSubTok;
+                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                    if (nt < kSubTok) {
+                        const int t0 = quad * 2;
+                        mlo = (t0 < nt ? 0x0000ffffu : 0u) | (t0 + 1 < nt ? 0xffff0000u : 0u);
+                        mhi = (t0 + 8 < nt ? 0x0000ffffu : 0u) | (t0 + 9 < nt ? 0xffff0000u : 0u);
+                    }
+                    // ---- O^T += V^T P^T: A = V^T (16 dims x 16 tokens per m-tile)
+#pragma unroll
+                    for (int j = 0; j < kMTiles; ++j) {
+                        const int chunk = ((j & 3) << 1) + k_dsub;
+                        uint32_t v0, v1, v2, v3;
+                        ldsm_x4_t(vbase + (j >> 2) * (kB * 128) + (u * kSubTok + k_tok) * 128 +
+                                      ((chunk ^ (k_tok & 7)) << 4),
+                                  v0, v1, v2, v3);
+                        v0 &= mlo; v1 &= mlo; v2 &= mhi; v3 &= mhi;
+                        mma_bf16_16816(ot[j], v0, v1, v2, v3, pb0, pb1);
+                    }
                 }
             }
             __syncwarp();
@@ -969,7 +1005,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
 // Pool [num_blocks][16][Hkv][D] bf16 seen as a 5-D tensor whose box is one
 // block for `box_heads` kv-heads, laid out in shared memory as
 // [head][D/64][token][64] with 128-byte rows and the 128-byte swizzle.
-CUresult make_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int D,
+CUresult make_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int B, int hkv, int D,
                        int box_heads, bool permuted) {
     auto encode = tensor_map_encoder();
     if (!encode) return CUDA_ERROR_NOT_FOUND;
@@ -980,12 +1016,12 @@ CUresult make_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int h
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     if (permuted) {
         // dims: d_lo(64), token(16), d_hi(D/64), head(Hkv), block
-        dims[0] = 64; dims[1] = kB; dims[2] = D / 64; dims[3] = hkv; dims[4] = num_blocks;
+        dims[0] = 64; dims[1] = B; dims[2] = D / 64; dims[3] = hkv; dims[4] = num_blocks;
         strides[0] = (cuuint64_t)hkv * D * eb;   // token
         strides[1] = 64 * eb;                     // d_hi
         strides[2] = (cuuint64_t)D * eb;          // head
-        strides[3] = (cuuint64_t)kB * hkv * D * eb;  // block
-        box[0] = 64; box[1] = kB; box[2] = D / 64; box[3] = box_heads; box[4] = 1;
+        strides[3] = (cuuint64_t)B * hkv * D * eb;   // block
+        box[0] = 64; box[1] = B; box[2] = D / 64; box[3] = box_heads; box[4] = 1;
     } else {
         return CUDA_ERROR_INVALID_VALUE;
     }
@@ -998,9 +1034,22 @@ struct Layout {
     int kvh, wpk, gw, group, qh, nhg;
 };
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory stages of the ring (up to 8) for one block of kvh kv-heads and
+// the CTA's qh query heads.
+int stages_for(int kvh, int qh, int D, int B) {
+    const int kv_tile = kvh * B * D * 2;
+    const int stage_bytes = (int)align_up(2 * kv_tile + qh * D * 2, 1024);
+    int ns = (kSmemBudget - 1024) / (stage_bytes + (int)sizeof(StageHeader) + 16);
+    return ns > 8 ? 8 : ns;
+}
+
 // kv-heads per CTA: up to 8 consumer warps of at most 8 q-heads each and up to
-// 32 q-heads in all, dividing the kv-heads evenly.
-Layout decode_layout(int num_heads, int num_kv_heads) {
+// 32 q-heads in all, dividing the kv-heads evenly, and few enough that a block
+// of B tokens leaves room for three stages (a block of 32 tokens x 8 kv-heads
+// x 128 dims would fill shared memory with one).
+Layout decode_layout(int num_heads, int num_kv_heads, int D, int B) {
     Layout L;
     L.group = num_heads / num_kv_heads;
     L.wpk = (L.group + kHeadsPerWarp - 1) / kHeadsPerWarp;
@@ -1008,14 +1057,14 @@ Layout decode_layout(int num_heads, int num_kv_heads) {
     int kvh = kMaxConsumerWarps / L.wpk;
     if (kvh > kMaxKvhPerCta) kvh = kMaxKvhPerCta;
     if (kvh > num_kv_heads) kvh = num_kv_heads;
-    while (kvh > 1 && (kvh * L.group > kMaxQHeadsPerCta || num_kv_heads % kvh != 0)) --kvh;
+    while (kvh > 1 && (kvh * L.group > kMaxQHeadsPerCta || num_kv_heads % kvh != 0 ||
+                       stages_for(kvh, kvh * L.group, D, B) < 3))
+        --kvh;
     L.kvh = kvh;
     L.qh = kvh * L.group;
     L.nhg = num_kv_heads / kvh;
     return L;
 }
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: the plan's prefix [S + 1] and SM split, the arrival counters of
 // cut sequences [kPartialCtas][kMaxConsumerWarps], the block stream [S * max_blocks],
@@ -1038,13 +1087,13 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int 
     return w;
 }
 
-template <int D>
+template <int D, int B>
 cudaError_t launch_main(const DecodeParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
                         int grid, cudaStream_t stream, bool timed) {
-    const int kv_tile = prm.kvh * kB * D * 2;
+    const int kv_tile = prm.kvh * B * D * 2;
     const int stage_bytes = (int)align_up(2 * kv_tile + prm.qh * D * 2, 1024);
     const size_t smem = 1024 + (size_t)prm.num_stages * (stage_bytes + sizeof(StageHeader) + 16);
-    auto kern = split_decode_kernel<D>;
+    auto kern = split_decode_kernel<D, B>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (timed) timing_begin(stream);
@@ -1053,25 +1102,20 @@ cudaError_t launch_main(const DecodeParams &prm, const CUtensorMap &mk, const CU
     return e;
 }
 
-int stages_for(int kvh, int qh, int D) {
-    const int kv_tile = kvh * kB * D * 2;
-    const int stage_bytes = (int)align_up(2 * kv_tile + qh * D * 2, 1024);
-    int ns = (kSmemBudget - 1024) / (stage_bytes + (int)sizeof(StageHeader) + 16);
-    return ns > 8 ? 8 : ns;
-}
+int log2_of_block(int B) { return B == 8 ? 3 : (B == 16 ? 4 : (B == 32 ? 5 : -1)); }
 
 }  // namespace
 
 bool split_decode_supported(const AttnArgs &a) {
-    if (a.dtype != PA_DTYPE_BF16 || a.block_size != kB) return false;
+    if (a.dtype != PA_DTYPE_BF16 || log2_of_block(a.block_size) < 0) return false;
     if (a.head_dim != 64 && a.head_dim != 128) return false;
     if (a.num_seqs > kMaxSeqs) return false;
     if ((int64_t)a.num_seqs * a.max_blocks >= (int64_t)1 << 30) return false;
     const int G = a.num_heads / a.num_kv_heads;
     if (G > kMaxGroup) return false;
-    const Layout L = decode_layout(a.num_heads, a.num_kv_heads);
+    const Layout L = decode_layout(a.num_heads, a.num_kv_heads, a.head_dim, a.block_size);
     if (L.qh > kMaxQHeadsPerCta) return false;
-    if (stages_for(L.kvh, L.qh, a.head_dim) < 2) return false;
+    if (stages_for(L.kvh, L.qh, a.head_dim, a.block_size) < 2) return false;
     auto al = [](const void *ptr, uintptr_t n) { return reinterpret_cast<uintptr_t>(ptr) % n == 0; };
     return al(a.q, 16) && al(a.k_cache, 16) && al(a.v_cache, 16) && al(a.out, 4);
 }
@@ -1089,7 +1133,8 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     const WorkspaceLayout w = workspace_layout(a.num_seqs, a.num_heads, a.head_dim, a.max_blocks);
     if (workspace_bytes < w.total) return cudaErrorInvalidValue;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const Layout L = decode_layout(a.num_heads, a.num_kv_heads);
+    const Layout L = decode_layout(a.num_heads, a.num_kv_heads, a.head_dim, a.block_size);
+    const int B = a.block_size;
 
     DecodeParams prm;
     prm.q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -1109,7 +1154,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.active = reinterpret_cast<const int32_t *>(ws + w.active);
     prm.arrivals = reinterpret_cast<int32_t *>(ws + w.arrivals);
     prm.shared_sms = prefill ? 1 : 0;
-    prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim);
+    prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim, B);
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.status = a.status;
     // decode calls (one query row per sequence, all CTAs take a slice): each
@@ -1131,12 +1176,12 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     // tensor maps: one TMA per block for all kv-heads of the CTA
     CUtensorMap mk, mv;
     prm.tma_heads = L.kvh;
-    if (make_pool_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, L.kvh, true) != CUDA_SUCCESS ||
-        make_pool_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, L.kvh, true) != CUDA_SUCCESS) {
+    if (make_pool_map(&mk, a.k_cache, a.num_blocks, B, a.num_kv_heads, a.head_dim, L.kvh, true) != CUDA_SUCCESS ||
+        make_pool_map(&mv, a.v_cache, a.num_blocks, B, a.num_kv_heads, a.head_dim, L.kvh, true) != CUDA_SUCCESS) {
         // one TMA per kv-head
         prm.tma_heads = 1;
-        if (make_pool_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1, true) != CUDA_SUCCESS ||
-            make_pool_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1, true) != CUDA_SUCCESS)
+        if (make_pool_map(&mk, a.k_cache, a.num_blocks, B, a.num_kv_heads, a.head_dim, 1, true) != CUDA_SUCCESS ||
+            make_pool_map(&mv, a.v_cache, a.num_blocks, B, a.num_kv_heads, a.head_dim, 1, true) != CUDA_SUCCESS)
             return cudaErrorNotSupported;
     }
 
@@ -1153,7 +1198,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
         job.v_cache = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
         job.slot_mapping = write->slot_mapping;
         job.row_vecs = a.num_kv_heads * a.head_dim * 2 / 16;
-        job.pool_slots = (int64_t)a.num_blocks * kB;
+        job.pool_slots = (int64_t)a.num_blocks * B;
     }
 
     // plan (and the folded cache write)
@@ -1173,7 +1218,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     split.grid = grid;
     split.share = share_sms ? 1 : 0;
     split.causal = a.causal;
-    split.block_ns = (double)kB * a.num_kv_heads * a.head_dim * 2 * 2 / kDecodeBytesPerSmNs;
+    split.block_ns = (double)B * a.num_kv_heads * a.head_dim * 2 * 2 / kDecodeBytesPerSmNs;
     split.pair_ns = 4.0 * a.num_heads * a.head_dim / kPrefillFlopsPerSmNs;
     int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
     if (plan_grid > 2 * sms) plan_grid = 2 * sms;
@@ -1189,12 +1234,19 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     const PrefillPlanJob pf = share_sms ? *prefill : PrefillPlanJob{};
     e = launch_dependent(plan_kern, dim3(plan_grid), dim3(kPlanThreads), plan_smem, stream,
                          a.context_lens, a.cu_seqlens_q, a.block_tables, a.num_seqs, a.max_blocks,
-                         a.num_blocks, a.total_q, reinterpret_cast<int32_t *>(ws + w.prefix),
+                         a.num_blocks, a.total_q, log2_of_block(B), reinterpret_cast<int32_t *>(ws + w.prefix),
                          reinterpret_cast<StreamEntry *>(ws + w.stream), a.status, job, split, pf);
     if (e != cudaSuccess) return e;
 
-    e = a.head_dim == 64 ? launch_main<64>(prm, mk, mv, grid, stream, timed)
-                         : launch_main<128>(prm, mk, mv, grid, stream, timed);
+    switch (a.head_dim * 100 + B) {
+        case 6408: e = launch_main<64, 8>(prm, mk, mv, grid, stream, timed); break;
+        case 6416: e = launch_main<64, 16>(prm, mk, mv, grid, stream, timed); break;
+        case 6432: e = launch_main<64, 32>(prm, mk, mv, grid, stream, timed); break;
+        case 12808: e = launch_main<128, 8>(prm, mk, mv, grid, stream, timed); break;
+        case 12816: e = launch_main<128, 16>(prm, mk, mv, grid, stream, timed); break;
+        case 12832: e = launch_main<128, 32>(prm, mk, mv, grid, stream, timed); break;
+        default: e = cudaErrorNotSupported;
+    }
     if (e != cudaSuccess) return e;
     return between ? (*between)() : cudaSuccess;
 }

@@ -38,11 +38,9 @@
 namespace pa {
 namespace {
 
-constexpr int kB = kBlockSize;
 constexpr int BM = 128;               // rows per M-tile
 constexpr int kMT = 2;                // M-tiles per CTA, one softmax warpgroup each
 constexpr int BN = 128;               // keys per KV tile (8 cache blocks)
-constexpr int kBlocksPerTile = BN / kB;
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kProducerWarp = 4 * kMT;
 constexpr int kMmaWarp = kProducerWarp + 1;
@@ -125,6 +123,7 @@ struct Item {
 };
 constexpr int kItemSlots = 4;                 // items published ahead of their use
 
+template <int kB>
 __device__ __forceinline__ Item decode_item(const PrefillParams &p, int w) {
     Item it;
     const int e = w / p.num_kv_heads;
@@ -151,11 +150,13 @@ __device__ __forceinline__ Item decode_item(const PrefillParams &p, int w) {
 // while the tensor pipe and the softmax warpgroups still finish the current
 // one; the K/V ring, the TMEM buffers and every barrier carry over from item
 // to item, their phases counted by running totals that all roles keep alike.
-template <int D>
+template <int D, int kB>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+    constexpr int kBlocksPerTile = BN / kB;          // cache blocks per KV tile
+    static_assert(kBlocksPerTile * (D / 64) <= 32, "one TMA box per producer lane");
     using SH = Shape<D>;
     constexpr int kDH = SH::kDH, kQBytes = SH::kQBytes, kSlotBytes = SH::kSlotBytes;
     constexpr int kPlaneQ = SH::kPlaneQ, kPlaneKV = SH::kPlaneKV, kSlots = SH::kSlots;
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             okp = __shfl_sync(kFull, okp ? 1 : 0, 0) != 0;
             w = __shfl_sync(kFull, w, 0);
             if (w < total) {
-                I = decode_item(p, w);
+                I = decode_item<kB>(p, w);
             } else {
                 I = Item{};
                 I.live = 0;
@@ -630,7 +631,7 @@ CUresult make_q_map(CUtensorMap *map, const void *q, int total_q, int num_heads,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-CUresult make_kv_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int D) {
+CUresult make_kv_map(CUtensorMap *map, const void *pool, int num_blocks, int kB, int hkv, int D) {
     auto encode = tensor_map_encoder();
     if (!encode) return CUDA_ERROR_NOT_FOUND;
     // dims: d_lo(64), token(16), d_hi(D/64), head(Hkv), block; box: one block,
@@ -654,11 +655,11 @@ int log2_exact(int v) {
     return (1 << s) == v ? s : -1;
 }
 
-template <int D>
+template <int D, int B>
 cudaError_t launch_main(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                         const PrefillParams &prm, int grid, cudaStream_t stream) {
     const size_t smem = Shape<D>::kSmem;
-    auto kern = prefill_kernel<D>;
+    auto kern = prefill_kernel<D, B>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -674,7 +675,8 @@ size_t plan_capacity(int num_seqs, int total_q) { return (size_t)total_q / 8 + n
 }  // namespace
 
 bool prefill_tc_supported(const AttnArgs &a) {
-    if (a.dtype != PA_DTYPE_BF16 || a.block_size != kB) return false;
+    if (a.dtype != PA_DTYPE_BF16) return false;
+    if (a.block_size != 8 && a.block_size != 16 && a.block_size != 32) return false;
     if (a.head_dim != 64 && a.head_dim != 128) return false;
     const int G = a.num_heads / a.num_kv_heads;
     if (G > 16 || log2_exact(G) < 0) return false;
@@ -713,8 +715,8 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
 
     CUtensorMap mq, mk, mv;
     if (make_q_map(&mq, a.q, a.total_q, a.num_heads, a.head_dim, pos, G) != CUDA_SUCCESS ||
-        make_kv_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS ||
-        make_kv_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS)
+        make_kv_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS ||
+        make_kv_map(&mv, a.v_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
 
     if (!planned) {
@@ -756,8 +758,15 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
     const size_t items = (size_t)job.capacity * (size_t)a.num_kv_heads;
     const int sms = device_sm_count();
     const int grid = (int)(items < (size_t)sms ? items : (size_t)sms);
-    return a.head_dim == 64 ? launch_main<64>(mq, mk, mv, prm, grid, stream)
-                            : launch_main<128>(mq, mk, mv, prm, grid, stream);
+    switch (a.head_dim * 100 + a.block_size) {
+        case 6408: return launch_main<64, 8>(mq, mk, mv, prm, grid, stream);
+        case 6416: return launch_main<64, 16>(mq, mk, mv, prm, grid, stream);
+        case 6432: return launch_main<64, 32>(mq, mk, mv, prm, grid, stream);
+        case 12808: return launch_main<128, 8>(mq, mk, mv, prm, grid, stream);
+        case 12816: return launch_main<128, 16>(mq, mk, mv, prm, grid, stream);
+        case 12832: return launch_main<128, 32>(mq, mk, mv, prm, grid, stream);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 }  // namespace pa

@@ -80,7 +80,7 @@ pa_status check_attention_shape(int num_seqs, int num_heads, int num_kv_heads, i
     if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN
     if (elem_bytes(dtype) == 0) return PA_ERR_INVALID_ARG;
-    if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > 32) return PA_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks * block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
@@ -147,7 +147,6 @@ pa_status pa_compute_slot_mapping(const int32_t *block_tables, int num_seqs, int
     if (total_new > 0 && num_seqs == 0) return PA_ERR_INVALID_ARG;
     if (total_new == 0) return PA_OK;
     if (!block_tables || !seq_start || !cu_seqlens_q || !slot_mapping) return PA_ERR_INVALID_ARG;
-    if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
     return from_cuda(launch_slot_mapping(block_tables, num_seqs, max_blocks, seq_start,
                                          cu_seqlens_q, total_new, block_size, num_blocks,
                                          slot_mapping, dev_status, (cudaStream_t)stream));
@@ -168,7 +167,6 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_s
     if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
     if (!aligned(key, eb) || !aligned(value, eb) || !aligned(k_cache, eb) || !aligned(v_cache, eb))
         return PA_ERR_INVALID_ARG;
-    if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
     return from_cuda(launch_reshape_and_cache(key, value, key_stride_tok, value_stride_tok,
                                               k_cache, v_cache, slot_mapping, num_tokens,
                                               num_kv_heads, head_dim, block_size, num_blocks, eb,

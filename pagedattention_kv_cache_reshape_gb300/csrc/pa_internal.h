@@ -39,7 +39,6 @@ struct AttnArgs {
     int causal = 1;  // 0: every query row sees all context_lens[s] keys (encode-only)
 };
 
-constexpr int kBlockSize = 16;     // tokens per cache block (the only one built)
 constexpr int kMaxPersistentCtas = 1024;
 
 int device_sm_count();  // SM count of the current device (cached per device)

@@ -180,20 +180,21 @@ def tiny(seed: int, blocks_needed: BlocksNeeded, device="cpu") -> Workload:
 
 
 def mha(seed: int, blocks_needed: BlocksNeeded, num_seqs: int = 64, ctx_lo: int = 128,
-        ctx_hi: int = 384, device="cpu") -> Workload:
+        ctx_hi: int = 384, block_size: int = 16, device="cpu") -> Workload:
     """LLaMA-2-7B-shaped MHA decode: 32 heads, head_dim 128, bf16, context U{lo..hi},
     pool 1.25x the used blocks."""
     rng = np.random.default_rng(seed + 1000)
     ctx = rng.integers(ctx_lo, ctx_hi + 1, size=num_seqs)
-    return build("mha64_bf16" if num_seqs == 64 and ctx_hi == 384 else f"mha_{num_seqs}",
+    name = "mha64_bf16" if num_seqs == 64 and ctx_hi == 384 else f"mha_{num_seqs}"
+    return build(name if block_size == 16 else f"{name}_b{block_size}",
                  seed=seed, blocks_needed=blocks_needed, dtype=torch.bfloat16,
-                 num_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
+                 num_heads=32, num_kv_heads=32, head_dim=128, block_size=block_size,
                  q_lens=np.ones(num_seqs, dtype=np.int64), context_lens=ctx, device=device)
 
 
 def gqa(seed: int, blocks_needed: BlocksNeeded, num_seqs: int = 256, ctx_lo: int = 16,
         ctx_hi: int = 4096, shared_seqs: int = 64, prefix_tokens: int = 1024,
-        device="cpu") -> Workload:
+        block_size: int = 16, device="cpu") -> Workload:
     """GQA decode at max_num_seqs: 32 q-heads / 8 kv-heads, head_dim 128, bf16, context
     power law x^-1.2 on [lo, hi]; sequences 0..shared_seqs-1 share a prefix_tokens
     system prompt (context = min(prefix + draw, hi))."""
@@ -201,15 +202,16 @@ def gqa(seed: int, blocks_needed: BlocksNeeded, num_seqs: int = 256, ctx_lo: int
     ctx = power_law_lengths(rng, num_seqs, 1.2, ctx_lo, ctx_hi)
     ctx[:shared_seqs] = np.minimum(prefix_tokens + ctx[:shared_seqs], ctx_hi)
     name = "gqa256_bf16" if (num_seqs, ctx_hi, shared_seqs) == (256, 4096, 64) else f"gqa_{num_seqs}"
-    return build(name, seed=seed, blocks_needed=blocks_needed, dtype=torch.bfloat16,
-                 num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    return build(name if block_size == 16 else f"{name}_b{block_size}",
+                 seed=seed, blocks_needed=blocks_needed, dtype=torch.bfloat16,
+                 num_heads=32, num_kv_heads=8, head_dim=128, block_size=block_size,
                  q_lens=np.ones(num_seqs, dtype=np.int64), context_lens=ctx,
                  shared_prefix_seqs=shared_seqs, shared_prefix_tokens=prefix_tokens, device=device)
 
 
 def mixed(seed: int, blocks_needed: BlocksNeeded, num_prefill: int = 8, chunk: int = 512,
           prefix_hi: int = 2048, num_decode: int = 248, dec_lo: int = 128, dec_hi: int = 2048,
-          device="cpu") -> Workload:
+          block_size: int = 16, device="cpu") -> Workload:
     """Mixed continuous-batching step: num_prefill chunks of `chunk` new tokens over
     U{0..prefix_hi} cached tokens plus num_decode decode rows with context U{lo..hi};
     the requests appear in a random order inside one super-sequence."""
@@ -220,18 +222,23 @@ def mixed(seed: int, blocks_needed: BlocksNeeded, num_prefill: int = 8, chunk: i
     ctx = np.concatenate([prefixes + chunk, dec_ctx])
     order = rng.permutation(q_lens.size)
     name = "mixed_bf16" if (num_prefill, chunk, num_decode) == (8, 512, 248) else f"mixed_{num_prefill}x{chunk}"
-    return build(name, seed=seed, blocks_needed=blocks_needed, dtype=torch.bfloat16,
-                 num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    return build(name if block_size == 16 else f"{name}_b{block_size}",
+                 seed=seed, blocks_needed=blocks_needed, dtype=torch.bfloat16,
+                 num_heads=32, num_kv_heads=8, head_dim=128, block_size=block_size,
                  q_lens=q_lens[order], context_lens=ctx[order], device=device)
 
 
 def long(seed: int, blocks_needed: BlocksNeeded, num_seqs: int = 16, ctx: int = 32768,
-         num_blocks: int = 36864, device="cpu") -> Workload:
+         num_blocks: Optional[int] = None, block_size: int = 16, device="cpu") -> Workload:
     """Long-context split-KV decode: 16 x 32768 context, 32/8 heads, head_dim 128,
-    bf16, 36,864-block pool, 1% of key rows scaled x8."""
+    bf16, 36,864-block pool (the same tokens at other block sizes), 1% of key
+    rows scaled x8."""
+    if num_blocks is None:
+        num_blocks = 36864 * 16 // block_size
     name = "long_bf16" if (num_seqs, ctx) == (16, 32768) else f"long_{num_seqs}x{ctx}"
-    return build(name, seed=seed, blocks_needed=blocks_needed, dtype=torch.bfloat16,
-                 num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    return build(name if block_size == 16 else f"{name}_b{block_size}",
+                 seed=seed, blocks_needed=blocks_needed, dtype=torch.bfloat16,
+                 num_heads=32, num_kv_heads=8, head_dim=128, block_size=block_size,
                  q_lens=np.ones(num_seqs, dtype=np.int64), context_lens=np.full(num_seqs, ctx),
                  num_blocks=num_blocks, key_outlier_frac=0.01, device=device)
 

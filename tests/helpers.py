@@ -23,7 +23,7 @@ def gpu_step(w: W.Workload, dev_status=None, out=None, workspace=None):
     """slot mapping -> cache write -> attention, all on the device.  Mutates the
     workload's device pools.  Returns (slots, out)."""
     slots = pa.compute_slot_mapping(w.block_tables, w.seq_start, w.cu_seqlens_q, w.num_blocks,
-                                    w.total_q, dev_status=dev_status)
+                                    w.total_q, block_size=w.block_size, dev_status=dev_status)
     pa.reshape_and_cache(w.key, w.value, w.k_cache, w.v_cache, slots, dev_status=dev_status)
     if w.decode_only:
         out = pa.decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,

@@ -68,16 +68,17 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.pa_compute_slot_mapping(nul, 1, 4, nul, nul, 0, 16, 8, nul, nul, nul) == pa.OK
     # cache write: token stride shorter than a row
     assert L.pa_reshape_and_cache(1, 1, 10, 64, 1, 1, 1, 3, 2, 32, 16, 8, 0, nul, nul) == pa.ERR_INVALID_ARG
-    # cache write: unsupported block size
-    assert L.pa_reshape_and_cache(16, 16, 64, 64, 16, 16, 16, 3, 2, 32, 8, 8, 0, nul, nul) == pa.ERR_UNSUPPORTED
+    # cache write: a block size below 1 (any positive block size is written)
+    assert L.pa_reshape_and_cache(16, 16, 64, 64, 16, 16, 16, 3, 2, 32, 0, 8, 0, nul, nul) == pa.ERR_INVALID_ARG
     # decode: heads not a multiple of kv-heads
     assert L.pa_decode(16, 16, 16, 16, 16, 16, 2, 6, 4, 128, 16, 4, 8, 0.1, 1, 16, 1 << 20, nul, nul) \
         == pa.ERR_INVALID_ARG
     # decode: unsupported head_dim / block size
     assert L.pa_decode(16, 16, 16, 16, 16, 16, 2, 8, 4, 96, 16, 4, 8, 0.1, 1, 16, 1 << 20, nul, nul) \
         == pa.ERR_UNSUPPORTED
-    assert L.pa_decode(16, 16, 16, 16, 16, 16, 2, 8, 4, 128, 32, 4, 8, 0.1, 1, 16, 1 << 20, nul, nul) \
-        == pa.ERR_UNSUPPORTED
+    for bs in (4, 24, 64):   # attention takes block sizes 8, 16 and 32
+        assert L.pa_decode(16, 16, 16, 16, 16, 16, 2, 8, 4, 128, bs, 4, 8, 0.1, 1, 16, 1 << 20, nul, nul) \
+            == pa.ERR_UNSUPPORTED
     # decode: bad dtype code, NaN scale, null pointer
     assert L.pa_decode(16, 16, 16, 16, 16, 16, 2, 8, 4, 128, 16, 4, 8, 0.1, 7, 16, 1 << 20, nul, nul) \
         == pa.ERR_INVALID_ARG

@@ -89,6 +89,40 @@ def test_17_token_prefill_spans_two_blocks():
     assert torch.isnan(pool[untouched]).all()
 
 
+@pytest.mark.parametrize("B", [8, 32])
+def test_prefill_lands_block_by_block_at_other_block_sizes(B):
+    """The same 17-token prefill at block size B (a setting of the engine):
+    token t lands at offset t % B of the table's block t // B, read back through
+    the pool's own indexing, and ceil(17 / B) blocks are touched."""
+    (n, _, _), = _golden("block_count.txt")
+    nb = oracle.num_blocks_needed(n, B)
+    assert nb == -(-n // B)
+    bt_row = [7, 2, 5][:nb]
+    slots, pool = _write_sequence(bt_row, 0, n, B, num_blocks=8)
+    for t in range(n):
+        assert pool[bt_row[t // B], t % B, 0, 0].item() == t + 1
+    written = (~torch.isnan(pool[:, :, 0, 0])).sum().item()
+    assert written == n
+    untouched = [b for b in range(8) if b not in bt_row]
+    assert torch.isnan(pool[untouched]).all()
+
+
+@pytest.mark.parametrize("B", [8, 32])
+def test_block_table_fill_at_other_block_sizes(B):
+    """The 24 tokens of the fill example at block size B fill min(B, 24 - iB)
+    tokens of logical block i, and the next token lands at logical block 24 // B,
+    offset 24 % B."""
+    n = sum(f for _, f in _golden("block_table_fill.txt"))
+    nb = oracle.num_blocks_needed(n + 1, B)
+    bt_row = [6, 1, 3, 4][:nb]
+    slots, pool = _write_sequence(bt_row, 0, n, B, num_blocks=8)
+    for logical, phys in enumerate(bt_row):
+        written = (~torch.isnan(pool[phys, :, 0, 0])).sum().item()
+        assert written == max(0, min(B, n - logical * B))
+    _, pool = _write_sequence(bt_row, n, 1, B, num_blocks=8, pool=pool)
+    assert pool[bt_row[n // B], n % B, 0, 0].item() == n + 1
+
+
 def test_block_table_fill_example():
     """A request with 24 tokens over three blocks has fill counts 16 / 8 / 0, and
     its next token lands in logical block 1 at offset 8."""
@@ -110,9 +144,10 @@ def test_block_table_fill_example():
     assert torch.isnan(pool[bt_row[2]]).all()
 
 
-def test_slot_mapping_injective_and_in_pool():
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_slot_mapping_injective_and_in_pool(B):
     rng = np.random.default_rng(7)
-    B, num_blocks = 16, 64
+    num_blocks = 64 * 16 // B + 8
     perm = rng.permutation(num_blocks).astype(np.int32)
     ctx = np.array([1, 15, 16, 17, 33, 100, 48])
     qlen = np.array([1, 15, 3, 17, 1, 36, 16])
@@ -250,10 +285,11 @@ def _oracle_out(P, nthreads=2):
 
 # ------------------------------------------------------------------ a4 / a6 pins
 
-@pytest.mark.parametrize("H,Hkv,D", [(4, 4, 64), (8, 2, 32), (6, 1, 16), (32, 8, 128)])
-def test_decode_matches_fp64_sdpa(H, Hkv, D):
-    ctx = [1, 16, 17, 50, 3, 64]
-    P = _dense_problem(11, ctx, [1] * len(ctx), H, Hkv, D)
+@pytest.mark.parametrize("H,Hkv,D,B", [(4, 4, 64, 16), (8, 2, 32, 16), (6, 1, 16, 16), (32, 8, 128, 16),
+                                       (8, 2, 32, 8), (8, 2, 32, 32), (32, 8, 128, 8), (32, 8, 128, 32)])
+def test_decode_matches_fp64_sdpa(H, Hkv, D, B):
+    ctx = [1, 16, 17, 50, 3, 64, 8, 9, 32, 33]
+    P = _dense_problem(11, ctx, [1] * len(ctx), H, Hkv, D, B=B)
     np.testing.assert_allclose(_oracle_out(P), _sdpa_reference(P), rtol=0, atol=1e-12)
 
 
@@ -265,12 +301,13 @@ def test_decode_without_cu_seqlens_equals_one_row_each():
     assert np.array_equal(a, b)
 
 
-def test_causal_prefill_matches_fp64_sdpa():
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_causal_prefill_matches_fp64_sdpa(B):
     # chunks over cached prefixes that do not start on a block boundary,
     # full prompts, and decode rows mixed in one super-sequence
     ctx = [40, 17, 1, 90, 33]
     qlen = [40, 5, 1, 37, 1]
-    P = _dense_problem(5, ctx, qlen, 8, 2, 64)
+    P = _dense_problem(5, ctx, qlen, 8, 2, 64, B=B)
     np.testing.assert_allclose(_oracle_out(P), _sdpa_reference(P), rtol=0, atol=1e-12)
 
 
@@ -294,15 +331,17 @@ def test_encode_only_matches_unmasked_fp64_sdpa():
         assert np.array_equal(out[r], causal[r])
 
 
-def test_closed_form_single_key_returns_value():
-    P = _dense_problem(21, [1, 1], [1, 1], 4, 4, 16)
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_closed_form_single_key_returns_value(B):
+    P = _dense_problem(21, [1, 1], [1, 1], 4, 4, 16, B=B)
     o = _oracle_out(P)
     for s in range(2):
         assert np.array_equal(o[s], P["Vs"][s][0].double().numpy())
 
 
-def test_closed_form_equal_logits_give_mean_value():
-    P = _dense_problem(22, [37, 5], [1, 1], 4, 2, 16)
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_closed_form_equal_logits_give_mean_value(B):
+    P = _dense_problem(22, [37, 5], [1, 1], 4, 2, 16, B=B)
     P["q"].zero_()                                   # every logit 0
     o = _oracle_out(P)
     for s in range(2):
@@ -335,8 +374,9 @@ def test_closed_form_dominant_key():
     np.testing.assert_allclose(out[0, 1], v7, rtol=0, atol=1e-9)
 
 
-def test_block_permutation_invariance():
-    P = _dense_problem(31, [50, 16, 77, 3], [1, 1, 4, 1], 8, 2, 32, extra_blocks=6)
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_block_permutation_invariance(B):
+    P = _dense_problem(31, [50, 16, 77, 3], [1, 1, 4, 1], 8, 2, 32, B=B, extra_blocks=6)
     base = _oracle_out(P)
     nblk = P["kpool"].shape[0]
     perm = torch.randperm(nblk, generator=torch.Generator().manual_seed(9))
@@ -383,9 +423,10 @@ def test_batch_order_independence():
     assert np.array_equal(out, base[rows.numpy()])
 
 
-def test_prefill_row_equals_decode_at_that_position():
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_prefill_row_equals_decode_at_that_position(B):
     n = 45
-    P = _dense_problem(61, [n], [n], 4, 2, 32)
+    P = _dense_problem(61, [n], [n], 4, 2, 32, B=B)
     pre = _oracle_out(P)
     for i in [0, 1, 15, 16, 17, 31, 44]:
         dec = oracle.paged_attention(P["q"][i:i + 1], P["kpool"], P["vpool"], P["bt"],
