@@ -681,8 +681,13 @@ def measure_configs(args, pa, dev, flush_l2, n):
     peak, _ = measured_peaks()
     tc_peak = measured_tflops()
     out = {}
-    for name in W.FULL_CONFIGS:
-        w = W.make(name, args.seed, pa.num_blocks_needed, device=dev)
+    # the five configurations, then the headline one at cache block sizes 8 and 32
+    makers = [(name, (lambda n=name: W.make(n, args.seed, pa.num_blocks_needed, device=dev)))
+              for name in W.FULL_CONFIGS]
+    makers += [(f"gqa256_bf16_block{B}", (lambda B=B: W.gqa(args.seed, pa.num_blocks_needed, block_size=B,
+                                                              device=dev))) for B in (8, 32)]
+    for name, make in makers:
+        w = make()
         r = StepRunner(pa, w, dev, 3, not args.no_graph)
         step_ms = r.time_steps(n, flush_l2)
         kern_ms = r.time_kernel(n, flush_l2)
