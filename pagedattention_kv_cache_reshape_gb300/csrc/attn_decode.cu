@@ -48,11 +48,12 @@
 namespace pa {
 namespace {
 
-// Block sizes (tokens per cache block) the fast decode takes: 8, 16 and 32.
-// A block is processed as max(1, B/16) sub-tiles of 16 tokens, the M of the
-// m16n8k16 products; at B = 8 the tile's upper 8 rows are masked like a
-// partly filled block's tail.
-constexpr int kSubTok = 16;
+// The decode streams 16-token units whatever the cache block size B (8, 16
+// or 32 tokens): a unit is one block at B = 16, half a block at B = 32 (one
+// TMA box at token offset 0 or 16) and two blocks at B = 8 (two 8-row boxes;
+// the consumer's ldmatrix rows address both).  A unit is a stage of the ring
+// and the M of the consumer's m16n8k16 products.
+constexpr int kU = 16;
 constexpr int kMaxKvhPerCta = 8;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxQHeadsPerCta = 32;
@@ -75,8 +76,8 @@ constexpr double kPrefillFlopsPerSmNs = 5900.0;
 struct __align__(16) StreamEntry {
     int32_t seq;
     int32_t qrow;    // query / output row of the sequence
-    int32_t blk;     // physical block id, -1 if the table entry was invalid
-    int32_t packed;  // ntok (bits 0..5) | last block of its sequence (bit 6) | logical block << 8
+    int32_t blk;     // physical block id (B = 8: the unit's first block), -1 if a table entry was invalid
+    int32_t packed;  // ntok (bits 0..5) | last unit of its sequence (bit 6) | B = 32: upper half (bit 7) | unit << 8
 };
 
 struct __align__(16) StageHeader {
@@ -89,6 +90,8 @@ struct DecodeParams {
     __nv_bfloat16 *out;
     const int32_t *prefix;     // [num_seqs + 1]
     const StreamEntry *stream; // [T]
+    const int32_t *stream_b1;  // [T], B = 8 only: the unit's second block (-1: past the sequence end)
+    int log2b;                 // log2 of the cache block size
     float *part_o;             // [slots][QH][D]
     float *part_ml;            // [slots][QH][2]
     int num_seqs;
@@ -123,7 +126,7 @@ struct DecodeParams {
 
 // Optional cache write folded into the plan kernel (pa_decode_step): for new
 // token t of sequence s (cu_new[s] <= t < cu_new[s+1]) at position
-// p = seq_start[s] + t - cu_new[s], slot = block_tables[s][p/16]*16 + p%16;
+// p = seq_start[s] + t - cu_new[s], slot = block_tables[s][p/B]*B + p%B;
 // the token's K and V rows are copied there with 16-byte vectors.
 struct KvWriteJob {
     const int32_t *seq_start;
@@ -170,7 +173,8 @@ __global__ void __launch_bounds__(kPlanThreads)
                        const int32_t *__restrict__ cu_seqlens_q,
                        const int32_t *__restrict__ block_tables, int num_seqs, int max_blocks,
                        int num_blocks, int total_q, int log2b, int32_t *__restrict__ prefix,
-                       StreamEntry *__restrict__ stream, int32_t *status, const KvWriteJob job,
+                       StreamEntry *__restrict__ stream, int32_t *__restrict__ stream_b1, int32_t *status,
+                       const KvWriteJob job,
                        const DecodeSplit split, const PrefillPlanJob prefill) {
     const int B = 1 << log2b;   // tokens per cache block
     extern __shared__ __align__(16) int32_t pref_s[];  // [num_seqs + 1]
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(kPlanThreads)
                 if (ctx <= 0 || (int64_t)ctx > (int64_t)max_blocks * B) {
                     if (blockIdx.x == 0) set_status(status, PA_ERR_OUT_OF_RANGE);
                 } else {
-                    nb = (ctx + B - 1) >> log2b;
+                    nb = (ctx + kU - 1) / kU;   // 16-token units
                 }
             }
         }
@@ -340,21 +344,38 @@ __global__ void __launch_bounds__(kPlanThreads)
             if (pref_s[mid] <= b) lo = mid; else hi = mid;
         }
         const int s = lo;
-        const int lb = b - pref_s[s];
+        const int lb = b - pref_s[s];            // 16-token unit of the sequence
         const int ctx = __ldg(context_lens + s);
-        int32_t blk = __ldg(block_tables + (int64_t)s * max_blocks + lb);
+        const int32_t *row = block_tables + (int64_t)s * max_blocks;
+        // the unit's physical block(s): B = 16 one, B = 32 half of one, B = 8 two
+        // (the second -1 past the sequence end; an invalid entry voids the unit)
+        int32_t blk, blk1 = -1;
+        int half = 0;
+        if (log2b == 4) {
+            blk = __ldg(row + lb);
+        } else if (log2b == 5) {
+            blk = __ldg(row + (lb >> 1));
+            half = lb & 1;
+        } else {
+            blk = __ldg(row + 2 * lb);
+            if ((2 * lb + 1) * 8 < ctx) {
+                blk1 = __ldg(row + 2 * lb + 1);
+                if (blk1 < 0 || blk1 >= num_blocks) blk = num_blocks;   // voids the unit below
+            }
+        }
         if (blk < 0 || blk >= num_blocks) {
             set_status(status, PA_ERR_OUT_OF_RANGE);
             blk = -1;
         }
-        const int ntok = min(B, ctx - lb * B);
-        const int seq_end = (lb + 1) * B >= ctx ? 1 : 0;
+        const int ntok = min(kU, ctx - lb * kU);
+        const int seq_end = (lb + 1) * kU >= ctx ? 1 : 0;
         StreamEntry e;
         e.seq = s;
         e.qrow = cu_seqlens_q ? __ldg(cu_seqlens_q + s) : s;
         e.blk = blk;
-        e.packed = ntok | (seq_end << 6) | (lb << 8);
+        e.packed = ntok | (seq_end << 6) | (half << 7) | (lb << 8);
         stream[b] = e;
+        if (log2b == 3) stream_b1[b] = blk1;
     }
 }
 
@@ -539,12 +560,13 @@ __device__ __forceinline__ void merge_group(const DecodeParams &p, int64_t slot0
 // consumer warps: the producer goes straight on to its wait and first
 // copies); they meet at named barrier 1.  warp_tot is shared memory for one
 // int per warp.
-template <int D, int kB>
+template <int D>
 __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int nblocks, int32_t *warp_tot,
                                                       int nthr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.num_seqs;
-    const int64_t max_tok = (int64_t)p.max_blocks * kB;
+    const int B = 1 << p.log2b;
+    const int64_t max_tok = (int64_t)p.max_blocks * B;
     // 1. blocks of this thread's contiguous range of sequences
     const int s0 = (int)((int64_t)S * tid / nthr), s1 = (int)((int64_t)S * (tid + 1) / nthr);
     int sum = 0;
@@ -554,7 +576,7 @@ __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int
         for (int u = 0; u < 8; ++u) c[u] = s + u < s1 ? __ldg(p.context_lens + s + u) : 0;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-            if (c[u] >= 1 && c[u] <= max_tok) sum += (c[u] + kB - 1) / kB;
+            if (c[u] >= 1 && c[u] <= max_tok) sum += (c[u] + kU - 1) / kU;
     }
     // 2. exclusive prefix over the threads' ranges
     int incl = sum;
@@ -587,21 +609,31 @@ __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int
         int acc = excl;
         for (int s = s0; s < s1; ++s) {
             const int ctx = __ldg(p.context_lens + s);
-            const int nb = (ctx >= 1 && ctx <= max_tok) ? (ctx + kB - 1) / kB : 0;
+            const int nb = (ctx >= 1 && ctx <= max_tok) ? (ctx + kU - 1) / kU : 0;
             if (b < acc + nb) {
-                const int32_t blk = __ldg(p.block_tables + (int64_t)s * p.max_blocks + (b - acc));
-                if (blk >= 0 && blk < p.num_blocks) {
-                    const int64_t base = (int64_t)blk * kB * row_bytes;
+                const int u = b - acc;   // the unit, and its rows of its block(s)
+                const int32_t *row = p.block_tables + (int64_t)s * p.max_blocks;
+                auto pf = [&](int32_t blk, int row0, int nrows) {
+                    if (blk < 0 || blk >= p.num_blocks) return;
+                    const int64_t base = ((int64_t)blk * B + row0) * row_bytes;
                     if (p.nhg == 1) {
-                        prefetch_l2_bulk(p.k_bytes + base, (uint32_t)(kB * row_bytes));
-                        prefetch_l2_bulk(p.v_bytes + base, (uint32_t)(kB * row_bytes));
+                        prefetch_l2_bulk(p.k_bytes + base, (uint32_t)(nrows * row_bytes));
+                        prefetch_l2_bulk(p.v_bytes + base, (uint32_t)(nrows * row_bytes));
                     } else {
                         const int64_t off = base + (int64_t)hg * span;
-                        for (int t = 0; t < kB; ++t) {
+                        for (int t = 0; t < nrows; ++t) {
                             prefetch_l2_bulk(p.k_bytes + off + t * row_bytes, span);
                             prefetch_l2_bulk(p.v_bytes + off + t * row_bytes, span);
                         }
                     }
+                };
+                if (p.log2b == 4) {
+                    pf(__ldg(row + u), 0, kU);
+                } else if (p.log2b == 5) {
+                    pf(__ldg(row + (u >> 1)), (u & 1) * kU, kU);
+                } else {
+                    pf(__ldg(row + 2 * u), 0, 8);
+                    if ((2 * u + 1) * 8 < ctx) pf(__ldg(row + 2 * u + 1), 0, 8);
                 }
                 break;
             }
@@ -611,13 +643,16 @@ __device__ __forceinline__ void prefetch_first_blocks(const DecodeParams &p, int
 }
 
 // ------------------------------------------------------------------ main kernel
-template <int D, int kB>
+// kTwo: the cache block size is 8, and a unit's K (and V) tile is two 8-row
+// TMA boxes, [box][kv-head][D/64 plane][8 rows][64], the second box kv_tile/2
+// bytes after the first; otherwise one 16-row box, [kv-head][plane][16 rows][64].
+template <int D, bool kTwo>
 __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     split_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-    constexpr int kHeadTileBytes = kB * D * 2;    // one kv-head of one block
+    constexpr int kHeadTileBytes = kU * D * 2;    // one kv-head of one unit
+    constexpr int kBoxRows = kTwo ? 8 : kU;       // token rows of one TMA box
     constexpr int kKSteps = D / 16;
-    constexpr int kSub = kB > kSubTok ? kB / kSubTok : 1;   // 16-token sub-tiles of a block
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -644,7 +679,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
-    if (p.context_lens && warp < cwarps) prefetch_first_blocks<D, kB>(p, NS, pf_warp_tot, 32 * cwarps);
+    if (p.context_lens && warp < cwarps) prefetch_first_blocks<D>(p, NS, pf_warp_tot, 32 * cwarps);
     grid_dependency_wait();      // the plan (and everything before it) is complete
     grid_dependents_launch();    // the next kernel may become resident
 
@@ -664,23 +699,25 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
         }
-        auto load_entry = [&](int64_t v, StreamEntry &e, int &hg) {
+        auto load_entry = [&](int64_t v, StreamEntry &e, int &hg, int &b1) {
+            b1 = -1;
             if (v < hi) {
                 hg = (int)(v / T);
                 e = p.stream[v - (int64_t)hg * T];
+                if (kTwo) b1 = p.stream_b1[v - (int64_t)hg * T];
             } else {
                 hg = -1;
                 e.seq = -1; e.qrow = 0; e.blk = -1; e.packed = 0;
             }
         };
         StreamEntry cur, nxt;
-        int cur_hg, nxt_hg;
-        load_entry(lo + lane, cur, cur_hg);
+        int cur_hg, nxt_hg, cur_b1, nxt_b1;
+        load_entry(lo + lane, cur, cur_hg, cur_b1);
         int prev_seq = -1, prev_hg = -1;
         int issued = 0;
         bool ok = true;
         for (int64_t base = lo; base < hi && ok; base += 32) {
-            load_entry(base + 32 + lane, nxt, nxt_hg);  // prefetch the next chunk
+            load_entry(base + 32 + lane, nxt, nxt_hg, nxt_b1);  // prefetch the next chunk
             const int n = (int)(hi - base < 32 ? hi - base : 32);
             const int next_seq_first = __shfl_sync(0xffffffffu, nxt.seq, 0);
             const int next_hg_first = __shfl_sync(0xffffffffu, nxt_hg, 0);
@@ -690,6 +727,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                 const int blk = __shfl_sync(0xffffffffu, cur.blk, i);
                 const int packed = __shfl_sync(0xffffffffu, cur.packed, i);
                 const int hg = __shfl_sync(0xffffffffu, cur_hg, i);
+                const int blk1 = kTwo ? __shfl_sync(0xffffffffu, cur_b1, i) : -1;
                 const int nseq = i + 1 < 32 ? __shfl_sync(0xffffffffu, cur.seq, (i + 1) & 31) : next_seq_first;
                 const int nhg = i + 1 < 32 ? __shfl_sync(0xffffffffu, cur_hg, (i + 1) & 31) : next_hg_first;
                 if (lane == 0) {
@@ -723,9 +761,24 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                         if (blk >= 0) {
                             const int h0 = hg * kvh;
                             for (int t = 0; t < kvh; t += p.tma_heads) {
-                                tma_load_5d(st + t * kHeadTileBytes, &tmap_k, 0, 0, 0, h0 + t, blk, full + stage);
-                                tma_load_5d(st + kv_tile + t * kHeadTileBytes, &tmap_v, 0, 0, 0, h0 + t, blk,
-                                            full + stage);
+                                if (kTwo) {
+                                    // two 8-token blocks; past the sequence end the coordinate
+                                    // num_blocks is out of bounds and TMA fills zeros
+                                    const int b1 = blk1 >= 0 ? blk1 : p.num_blocks;
+                                    const int ho = t * (8 * D * 2);
+                                    tma_load_5d(st + ho, &tmap_k, 0, 0, 0, h0 + t, blk, full + stage);
+                                    tma_load_5d(st + kv_tile / 2 + ho, &tmap_k, 0, 0, 0, h0 + t, b1, full + stage);
+                                    tma_load_5d(st + kv_tile + ho, &tmap_v, 0, 0, 0, h0 + t, blk, full + stage);
+                                    tma_load_5d(st + kv_tile + kv_tile / 2 + ho, &tmap_v, 0, 0, 0, h0 + t, b1,
+                                                full + stage);
+                                } else {
+                                    // 16 tokens from token tok0 of the block (B = 32: its upper half)
+                                    const int tok0 = ((packed >> 7) & 1) * kU;
+                                    tma_load_5d(st + t * kHeadTileBytes, &tmap_k, 0, tok0, 0, h0 + t, blk,
+                                                full + stage);
+                                    tma_load_5d(st + kv_tile + t * kHeadTileBytes, &tmap_v, 0, tok0, 0, h0 + t, blk,
+                                                full + stage);
+                                }
                             }
                         }
                         if (first) {
@@ -743,6 +796,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
             }
             cur = nxt;
             cur_hg = nxt_hg;
+            cur_b1 = nxt_b1;
         }
         // wait (bounded, always at the default limit) until every copy this CTA
         // issued has landed
@@ -815,39 +869,29 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                 piece_lb0 = h.lb;
             }
             if (h.flags & kValid) {
-                const uint32_t kbase = smem_u32(st + kh * kHeadTileBytes);
-                const uint32_t vbase = smem_u32(st + kv_tile + kh * kHeadTileBytes);
+                // byte address of token row t (0..15), 64-column plane pl, of this
+                // warp's kv-head in the K (or V) tile at `tile`
+                const uint32_t ktile = smem_u32(st), vtile = ktile + kv_tile;
+                auto row_addr = [&](uint32_t tile, int pl, int t) -> uint32_t {
+                    if (kTwo)
+                        return tile + (t >> 3) * (kv_tile >> 1) + kh * (8 * D * 2) + pl * (8 * 128) + (t & 7) * 128;
+                    return tile + kh * kHeadTileBytes + pl * (kBoxRows * 128) + t * 128;
+                };
+                // ---- S^T = K Q^T: A = K (tokens x 16 dims per step), B = Q^T
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < kKSteps; ++ks) {
+                    const int chunk = ((ks & 3) << 1) + v_dsub;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(row_addr(ktile, ks >> 2, v_tok) + ((chunk ^ (v_tok & 7)) << 4), a0, a1, a2, a3);
+                    mma_bf16_16816(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+                // ---- online softmax per head column (heads 2q, 2q+1; tokens r, r+8)
                 const int ntok = h.ntok;
-                // sub-tiles past the valid tokens (a partly filled block of 32) are skipped
-                const int nsub = kSub == 1 ? 1 : (ntok + kSubTok - 1) / kSubTok;
-                // ---- S^T = K Q^T per 16-token sub-tile: A = K (tokens x 16 dims per step), B = Q^T
-                float x[kSub][4];
+                float x[4];
 #pragma unroll
-                for (int u = 0; u < kSub; ++u) {
-                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (u < nsub) {
-#pragma unroll
-                        for (int ks = 0; ks < kKSteps; ++ks) {
-                            const int chunk = ((ks & 3) << 1) + v_dsub;
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(kbase + (ks >> 2) * (kB * 128) + (u * kSubTok + v_tok) * 128 +
-                                        ((chunk ^ (v_tok & 7)) << 4),
-                                    a0, a1, a2, a3);
-                            mma_bf16_16816(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-                        }
-                    }
-                    // tokens past ntok (the block's tail, or rows 8-15 of an 8-token block) are masked
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        x[u][i] = (u * kSubTok + r + (i >> 1) * 8) < ntok ? s4[i] * p.scale_log2 : -INFINITY;
-                }
-                // ---- online softmax per head column (heads 2q, 2q+1; tokens r, r+8 of each sub-tile)
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int u = 0; u < kSub; ++u) {
-                    mx0 = fmax3(mx0, x[u][0], x[u][2]);
-                    mx1 = fmax3(mx1, x[u][1], x[u][3]);
-                }
+                for (int i = 0; i < 4; ++i) x[i] = (r + (i >> 1) * 8) < ntok ? s4[i] * p.scale_log2 : -INFINITY;
+                float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -856,19 +900,10 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                 // ntok >= 1, so every column has a finite max
                 const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
                 const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
-                float pr[kSub][4];
-                float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-                for (int u = 0; u < kSub; ++u) {
-                    pr[u][0] = fast_exp2(x[u][0] - mn0);
-                    pr[u][1] = fast_exp2(x[u][1] - mn1);
-                    pr[u][2] = fast_exp2(x[u][2] - mn0);
-                    pr[u][3] = fast_exp2(x[u][3] - mn1);
-                    ls0 += pr[u][0] + pr[u][2];
-                    ls1 += pr[u][1] + pr[u][3];
-                }
-                l_part[0] = l_part[0] * al0 + ls0;
-                l_part[1] = l_part[1] * al1 + ls1;
+                const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
+                const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
+                l_part[0] = l_part[0] * al0 + (p0 + p2);
+                l_part[1] = l_part[1] * al1 + (p1 + p3);
                 m_run[0] = mn0;
                 m_run[1] = mn1;
 #pragma unroll
@@ -878,31 +913,24 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                     ot[j][2] *= al0;
                     ot[j][3] *= al1;
                 }
+                // P^T as the B operand: (token, head) pairs transposed to (head, token)
+                const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));   // tokens 0..7
+                const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));   // tokens 8..15
+                // masks for value rows past the sequence end (they may hold anything)
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (ntok < kU) {
+                    const int t0 = quad * 2;
+                    mlo = (t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u);
+                    mhi = (t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u);
+                }
+                // ---- O^T += V^T P^T: A = V^T (16 dims x 16 tokens per m-tile)
 #pragma unroll
-                for (int u = 0; u < kSub; ++u) {
-                    if (u >= nsub) break;
-                    // P^T as the B operand: (token, head) pairs transposed to (head, token)
-                    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(pr[u][0], pr[u][1]));   // tokens 0..7
-                    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(pr[u][2], pr[u][3]));   // tokens 8..15
-                    // masks for value rows past the valid tokens (they may hold anything)
-                    const int nt = ntok - u * kSubTok;
-                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                    if (nt < kSubTok) {
-                        const int t0 = quad * 2;
-                        mlo = (t0 < nt ? 0x0000ffffu : 0u) | (t0 + 1 < nt ? 0xffff0000u : 0u);
-                        mhi = (t0 + 8 < nt ? 0x0000ffffu : 0u) | (t0 + 9 < nt ? 0xffff0000u : 0u);
-                    }
-                    // ---- O^T += V^T P^T: A = V^T (16 dims x 16 tokens per m-tile)
-#pragma unroll
-                    for (int j = 0; j < kMTiles; ++j) {
-                        const int chunk = ((j & 3) << 1) + k_dsub;
-                        uint32_t v0, v1, v2, v3;
-                        ldsm_x4_t(vbase + (j >> 2) * (kB * 128) + (u * kSubTok + k_tok) * 128 +
-                                      ((chunk ^ (k_tok & 7)) << 4),
-                                  v0, v1, v2, v3);
-                        v0 &= mlo; v1 &= mlo; v2 &= mhi; v3 &= mhi;
-                        mma_bf16_16816(ot[j], v0, v1, v2, v3, pb0, pb1);
-                    }
+                for (int j = 0; j < kMTiles; ++j) {
+                    const int chunk = ((j & 3) << 1) + k_dsub;
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(row_addr(vtile, j >> 2, k_tok) + ((chunk ^ (k_tok & 7)) << 4), v0, v1, v2, v3);
+                    v0 &= mlo; v1 &= mlo; v2 &= mhi; v3 &= mhi;
+                    mma_bf16_16816(ot[j], v0, v1, v2, v3, pb0, pb1);
                 }
             }
             __syncwarp();
@@ -1002,9 +1030,9 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
 }
 
 // ------------------------------------------------------------------ host side
-// Pool [num_blocks][16][Hkv][D] bf16 seen as a 5-D tensor whose box is one
-// block for `box_heads` kv-heads, laid out in shared memory as
-// [head][D/64][token][64] with 128-byte rows and the 128-byte swizzle.
+// Pool [num_blocks][B][Hkv][D] bf16 seen as a 5-D tensor whose box is
+// min(B, 16) tokens of one block for `box_heads` kv-heads, laid out in shared
+// memory as [head][D/64][token][64] with 128-byte rows and the 128-byte swizzle.
 CUresult make_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int B, int hkv, int D,
                        int box_heads, bool permuted) {
     auto encode = tensor_map_encoder();
@@ -1015,13 +1043,13 @@ CUresult make_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int B
     cuuint32_t box[5];
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     if (permuted) {
-        // dims: d_lo(64), token(16), d_hi(D/64), head(Hkv), block
+        // dims: d_lo(64), token(B), d_hi(D/64), head(Hkv), block
         dims[0] = 64; dims[1] = B; dims[2] = D / 64; dims[3] = hkv; dims[4] = num_blocks;
         strides[0] = (cuuint64_t)hkv * D * eb;   // token
         strides[1] = 64 * eb;                     // d_hi
         strides[2] = (cuuint64_t)D * eb;          // head
         strides[3] = (cuuint64_t)B * hkv * D * eb;   // block
-        box[0] = 64; box[1] = B; box[2] = D / 64; box[3] = box_heads; box[4] = 1;
+        box[0] = 64; box[1] = B < kU ? B : kU; box[2] = D / 64; box[3] = box_heads; box[4] = 1;
     } else {
         return CUDA_ERROR_INVALID_VALUE;
     }
@@ -1036,20 +1064,19 @@ struct Layout {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Shared-memory stages of the ring (up to 8) for one block of kvh kv-heads and
-// the CTA's qh query heads.
-int stages_for(int kvh, int qh, int D, int B) {
-    const int kv_tile = kvh * B * D * 2;
+// Shared-memory stages of the ring (up to 8) for one 16-token unit of kvh
+// kv-heads and the CTA's qh query heads.
+int stages_for(int kvh, int qh, int D) {
+    const int kv_tile = kvh * kU * D * 2;
     const int stage_bytes = (int)align_up(2 * kv_tile + qh * D * 2, 1024);
     int ns = (kSmemBudget - 1024) / (stage_bytes + (int)sizeof(StageHeader) + 16);
     return ns > 8 ? 8 : ns;
 }
 
 // kv-heads per CTA: up to 8 consumer warps of at most 8 q-heads each and up to
-// 32 q-heads in all, dividing the kv-heads evenly, and few enough that a block
-// of B tokens leaves room for three stages (a block of 32 tokens x 8 kv-heads
-// x 128 dims would fill shared memory with one).
-Layout decode_layout(int num_heads, int num_kv_heads, int D, int B) {
+// 32 q-heads in all, dividing the kv-heads evenly, and few enough that a unit
+// leaves room for three stages.
+Layout decode_layout(int num_heads, int num_kv_heads, int D) {
     Layout L;
     L.group = num_heads / num_kv_heads;
     L.wpk = (L.group + kHeadsPerWarp - 1) / kHeadsPerWarp;
@@ -1058,7 +1085,7 @@ Layout decode_layout(int num_heads, int num_kv_heads, int D, int B) {
     if (kvh > kMaxKvhPerCta) kvh = kMaxKvhPerCta;
     if (kvh > num_kv_heads) kvh = num_kv_heads;
     while (kvh > 1 && (kvh * L.group > kMaxQHeadsPerCta || num_kv_heads % kvh != 0 ||
-                       stages_for(kvh, kvh * L.group, D, B) < 3))
+                       stages_for(kvh, kvh * L.group, D) < 3))
         --kvh;
     L.kvh = kvh;
     L.qh = kvh * L.group;
@@ -1066,34 +1093,40 @@ Layout decode_layout(int num_heads, int num_kv_heads, int D, int B) {
     return L;
 }
 
+// 16-token units of a sequence of max_blocks blocks of B tokens.
+int64_t max_units(int max_blocks, int B) { return ((int64_t)max_blocks * B + kU - 1) / kU; }
+
 // Workspace: the plan's prefix [S + 1] and SM split, the arrival counters of
-// cut sequences [kPartialCtas][kMaxConsumerWarps], the block stream [S * max_blocks],
-// then the partials, slot = hg*S + s + CTA (< NHG*S + CTAs): (m, l)
-// [slots][QH][2] and o [slots][QH][D], fp32.
+// cut sequences [kPartialCtas][kMaxConsumerWarps], the unit stream
+// [S * max units] (B = 8: and its second blocks), then the partials,
+// slot = hg*S + s + CTA (< NHG*S + CTAs): (m, l) [slots][QH][2] and
+// o [slots][QH][D], fp32.
 struct WorkspaceLayout {
-    size_t prefix, active, arrivals, stream, part_ml, part_o, total;
+    size_t prefix, active, arrivals, stream, stream_b1, part_ml, part_o, total;
 };
 
-WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_blocks) {
+WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_blocks, int B) {
     WorkspaceLayout w;
     const size_t slots_heads = ((size_t)num_seqs + kPartialCtas) * num_heads;
+    const size_t units = (size_t)num_seqs * (size_t)max_units(max_blocks, B);
     w.prefix = 0;
     w.active = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 16);
     w.arrivals = align_up(w.active + sizeof(int32_t), 256);
     w.stream = align_up(w.arrivals + sizeof(int32_t) * kPartialCtas * kMaxConsumerWarps, 256);
-    w.part_ml = align_up(w.stream + sizeof(StreamEntry) * (size_t)num_seqs * max_blocks, 256);
+    w.stream_b1 = align_up(w.stream + sizeof(StreamEntry) * units, 256);
+    w.part_ml = align_up(w.stream_b1 + (B < kU ? sizeof(int32_t) * units : 0), 256);
     w.part_o = align_up(w.part_ml + sizeof(float) * 2 * slots_heads, 256);
     w.total = align_up(w.part_o + sizeof(float) * (size_t)head_dim * slots_heads, 256);
     return w;
 }
 
-template <int D, int B>
+template <int D, bool kTwo>
 cudaError_t launch_main(const DecodeParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
                         int grid, cudaStream_t stream, bool timed) {
-    const int kv_tile = prm.kvh * B * D * 2;
+    const int kv_tile = prm.kvh * kU * D * 2;
     const int stage_bytes = (int)align_up(2 * kv_tile + prm.qh * D * 2, 1024);
     const size_t smem = 1024 + (size_t)prm.num_stages * (stage_bytes + sizeof(StageHeader) + 16);
-    auto kern = split_decode_kernel<D, B>;
+    auto kern = split_decode_kernel<D, kTwo>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (timed) timing_begin(stream);
@@ -1110,18 +1143,20 @@ bool split_decode_supported(const AttnArgs &a) {
     if (a.dtype != PA_DTYPE_BF16 || log2_of_block(a.block_size) < 0) return false;
     if (a.head_dim != 64 && a.head_dim != 128) return false;
     if (a.num_seqs > kMaxSeqs) return false;
-    if ((int64_t)a.num_seqs * a.max_blocks >= (int64_t)1 << 30) return false;
+    // a stream entry holds unit << 8: units of a sequence stay below 2^23
+    if (max_units(a.max_blocks, a.block_size) >= (int64_t)1 << 23) return false;
+    if ((int64_t)a.num_seqs * max_units(a.max_blocks, a.block_size) >= (int64_t)1 << 30) return false;
     const int G = a.num_heads / a.num_kv_heads;
     if (G > kMaxGroup) return false;
-    const Layout L = decode_layout(a.num_heads, a.num_kv_heads, a.head_dim, a.block_size);
+    const Layout L = decode_layout(a.num_heads, a.num_kv_heads, a.head_dim);
     if (L.qh > kMaxQHeadsPerCta) return false;
-    if (stages_for(L.kvh, L.qh, a.head_dim, a.block_size) < 2) return false;
+    if (stages_for(L.kvh, L.qh, a.head_dim) < 2) return false;
     auto al = [](const void *ptr, uintptr_t n) { return reinterpret_cast<uintptr_t>(ptr) % n == 0; };
     return al(a.q, 16) && al(a.k_cache, 16) && al(a.v_cache, 16) && al(a.out, 4);
 }
 
-size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max_blocks) {
-    return workspace_layout(num_seqs, num_heads, head_dim, max_blocks).total;
+size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max_blocks, int block_size) {
+    return workspace_layout(num_seqs, num_heads, head_dim, max_blocks, block_size).total;
 }
 
 cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t workspace_bytes,
@@ -1130,17 +1165,19 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
                                 const std::function<cudaError_t()> *between) {
     const bool share_sms = prefill != nullptr;
     if (a.num_seqs == 0) return cudaSuccess;
-    const WorkspaceLayout w = workspace_layout(a.num_seqs, a.num_heads, a.head_dim, a.max_blocks);
+    const int B = a.block_size;
+    const WorkspaceLayout w = workspace_layout(a.num_seqs, a.num_heads, a.head_dim, a.max_blocks, B);
     if (workspace_bytes < w.total) return cudaErrorInvalidValue;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const Layout L = decode_layout(a.num_heads, a.num_kv_heads, a.head_dim, a.block_size);
-    const int B = a.block_size;
+    const Layout L = decode_layout(a.num_heads, a.num_kv_heads, a.head_dim);
 
     DecodeParams prm;
     prm.q = static_cast<const __nv_bfloat16 *>(a.q);
     prm.out = static_cast<__nv_bfloat16 *>(a.out);
     prm.prefix = reinterpret_cast<const int32_t *>(ws + w.prefix);
     prm.stream = reinterpret_cast<const StreamEntry *>(ws + w.stream);
+    prm.stream_b1 = reinterpret_cast<const int32_t *>(ws + w.stream_b1);
+    prm.log2b = log2_of_block(B);
     prm.part_ml = reinterpret_cast<float *>(ws + w.part_ml);
     prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
     prm.num_seqs = a.num_seqs;
@@ -1154,7 +1191,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.active = reinterpret_cast<const int32_t *>(ws + w.active);
     prm.arrivals = reinterpret_cast<int32_t *>(ws + w.arrivals);
     prm.shared_sms = prefill ? 1 : 0;
-    prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim, B);
+    prm.num_stages = stages_for(L.kvh, L.qh, a.head_dim);
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.status = a.status;
     // decode calls (one query row per sequence, all CTAs take a slice): each
@@ -1207,7 +1244,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     auto plan_kern = share_sms ? decode_plan_kernel<true> : decode_plan_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(plan_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
     if (e != cudaSuccess) return e;
-    const int64_t max_entries = (int64_t)a.num_seqs * a.max_blocks;
+    const int64_t max_entries = (int64_t)a.num_seqs * max_units(a.max_blocks, B);
     const int sms = device_sm_count();
     int grid = sms;
     if (grid > kPartialCtas) grid = kPartialCtas;
@@ -1218,7 +1255,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     split.grid = grid;
     split.share = share_sms ? 1 : 0;
     split.causal = a.causal;
-    split.block_ns = (double)B * a.num_kv_heads * a.head_dim * 2 * 2 / kDecodeBytesPerSmNs;
+    split.block_ns = (double)kU * a.num_kv_heads * a.head_dim * 2 * 2 / kDecodeBytesPerSmNs;
     split.pair_ns = 4.0 * a.num_heads * a.head_dim / kPrefillFlopsPerSmNs;
     int plan_grid = (int)((max_entries + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
     if (plan_grid > 2 * sms) plan_grid = 2 * sms;
@@ -1235,18 +1272,15 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     e = launch_dependent(plan_kern, dim3(plan_grid), dim3(kPlanThreads), plan_smem, stream,
                          a.context_lens, a.cu_seqlens_q, a.block_tables, a.num_seqs, a.max_blocks,
                          a.num_blocks, a.total_q, log2_of_block(B), reinterpret_cast<int32_t *>(ws + w.prefix),
-                         reinterpret_cast<StreamEntry *>(ws + w.stream), a.status, job, split, pf);
+                         reinterpret_cast<StreamEntry *>(ws + w.stream), reinterpret_cast<int32_t *>(ws + w.stream_b1),
+                         a.status, job, split, pf);
     if (e != cudaSuccess) return e;
 
-    switch (a.head_dim * 100 + B) {
-        case 6408: e = launch_main<64, 8>(prm, mk, mv, grid, stream, timed); break;
-        case 6416: e = launch_main<64, 16>(prm, mk, mv, grid, stream, timed); break;
-        case 6432: e = launch_main<64, 32>(prm, mk, mv, grid, stream, timed); break;
-        case 12808: e = launch_main<128, 8>(prm, mk, mv, grid, stream, timed); break;
-        case 12816: e = launch_main<128, 16>(prm, mk, mv, grid, stream, timed); break;
-        case 12832: e = launch_main<128, 32>(prm, mk, mv, grid, stream, timed); break;
-        default: e = cudaErrorNotSupported;
-    }
+    const bool two = B < kU;   // B = 8: two blocks per unit
+    if (a.head_dim == 64) e = two ? launch_main<64, true>(prm, mk, mv, grid, stream, timed)
+                                  : launch_main<64, false>(prm, mk, mv, grid, stream, timed);
+    else e = two ? launch_main<128, true>(prm, mk, mv, grid, stream, timed)
+                 : launch_main<128, false>(prm, mk, mv, grid, stream, timed);
     if (e != cudaSuccess) return e;
     return between ? (*between)() : cudaSuccess;
 }

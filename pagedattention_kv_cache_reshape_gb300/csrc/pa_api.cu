@@ -107,7 +107,7 @@ pa_status decode_requirements(const void *out, const void *q, const void *k_cach
                num_seqs, num_seqs, 1, num_heads, num_kv_heads, head_dim, block_size,
                max_blocks, num_blocks, scale, dtype, nullptr};
     if (split_decode_supported(a))
-        *need = split_decode_workspace(num_seqs, num_heads, head_dim, max_blocks);
+        *need = split_decode_workspace(num_seqs, num_heads, head_dim, max_blocks, block_size);
     return PA_OK;
 }
 
@@ -176,12 +176,12 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_s
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks) {
     (void)num_kv_heads;
-    (void)block_size;
     if (num_seqs < 0) num_seqs = 0;
     if (num_heads < 1) num_heads = 1;
     if (head_dim < 1) head_dim = 1;
     if (max_blocks < 1) max_blocks = 1;
-    return split_decode_workspace(num_seqs, num_heads, head_dim, max_blocks);
+    if (block_size < 1) block_size = 1;
+    return split_decode_workspace(num_seqs, num_heads, head_dim, max_blocks, block_size);
 }
 
 pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,

@@ -97,7 +97,7 @@ pa_status decode_requirements(const void *out, const void *q, const void *k_cach
 
 // Persistent TMA + tensor-core split-KV decode (bf16, head_dim 64/128).
 bool split_decode_supported(const AttnArgs &a);
-size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max_blocks);
+size_t split_decode_workspace(int num_seqs, int num_heads, int head_dim, int max_blocks, int block_size);
 // Cache write folded into the decode plan kernel (bf16 rows of 16-byte
 // multiples, 16-byte aligned pointers and strides).
 struct KvWriteArgs {
