@@ -31,6 +31,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "prefill_plan.cuh"
@@ -160,6 +162,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     using SH = Shape<D>;
     constexpr int kDH = SH::kDH, kQBytes = SH::kQBytes, kSlotBytes = SH::kSlotBytes;
     constexpr int kPlaneQ = SH::kPlaneQ, kPlaneKV = SH::kPlaneKV, kSlots = SH::kSlots;
+    // V tile layout, block-major: [block][D/64 plane][B rows][64], one TMA box
+    // per block for all planes (K needs one box per block and plane: its
+    // K-major operand wants the 128 keys of a plane at one row pitch).  Key k
+    // sits at (k / B) * kVBlockBytes + (k % B) * 128 in a plane; 16-key MMA steps
+    // 0..3 of 64 keys start at 0, kVS1, kVS2 and kVS2 + kVS1; their 8-row groups
+    // are kVSbo apart and their planes B*128.
+    constexpr int kVBlockBytes = kDH * kB * 128;                       // one block, all planes
+    constexpr int kVS1 = (16 / kB) * kVBlockBytes + (16 % kB) * 128;
+    constexpr int kVS2 = (32 / kB) * kVBlockBytes + (32 % kB) * 128;
+    static_assert(((48 / kB) * kVBlockBytes + (48 % kB) * 128) == kVS1 + kVS2, "step 3 = s2 + s1");
+    constexpr int kVChunk = 64 / kB * kVBlockBytes;                    // 64 keys
+    constexpr int kVLbo = kB * 128;
+    constexpr int kVSbo = kB < 16 ? kVBlockBytes : 1024;
     constexpr uint32_t kIdescQK = umma_idesc_bf16(BM, BN, 0);
     constexpr uint32_t kIdescPV = umma_idesc_bf16(BM, D, 1);
     constexpr uint32_t kFull = 0xffffffffu;
@@ -321,9 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++chunk_cur;
                     ids_next = load_ids(chunk_cur + 1);
                 }
-                // lane (block b, plane dh) copies one 16-row box of K, then of V
+                // lane (block b, plane dh) copies one box of K (one plane of one
+                // block); V block-major: lane b < kBlocksPerTile copies block b
                 const int b = lane / kDH, dh = lane % kDH;
-                const int cb = __shfl_sync(kFull, ids_cur, ((j * kBlocksPerTile) & 31) + (b & (kBlocksPerTile - 1)));
+                const int id0 = (j * kBlocksPerTile) & 31;
+                const int cb = __shfl_sync(kFull, ids_cur, id0 + (b & (kBlocksPerTile - 1)));
+                const int cbv = __shfl_sync(kFull, ids_cur, id0 + (lane & (kBlocksPerTile - 1)));
                 for (int kv = 0; kv < 2; ++kv) {
                     const int m = n + 2 * j + kv;
                     if (p.stall == PA_STALL_PRODUCER && m >= p.stall_after) {
@@ -337,9 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (lane == 0) mbar_arrive_expect_tx(kv_full + slot_of(m), kSlotBytes);
                     __syncwarp();
-                    if (lane < kBlocksPerTile * kDH)
+                    if (kv) {
+                        if (lane < kBlocksPerTile)
+                            tma_load_5d(kv_s + slot_of(m) * kSlotBytes + lane * kVBlockBytes, &tmap_v, 0, 0, 0, I.g,
+                                        cbv, kv_full + slot_of(m));
+                    } else if (lane < kBlocksPerTile * kDH) {
                         tma_load_5d(kv_s + slot_of(m) * kSlotBytes + dh * kPlaneKV + b * (kB * 128),
                                     kv ? &tmap_v : &tmap_k, 0, 0, dh, I.g, cb, kv_full + slot_of(m));
+                    }
                     issued_end = m + 1;
                 }
             }
@@ -369,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // descriptors: constant fields + (address >> 4) in bits 0..13
         const uint64_t dq = umma_desc_sw128(q_addr, 16, 1024);
         const uint64_t dk = umma_desc_sw128(kv_addr, 16, 1024);
-        const uint64_t dv = umma_desc_sw128(kv_addr, kPlaneKV, 1024);
+        const uint64_t dv = umma_desc_sw128(kv_addr, kVLbo, kVSbo);
         // The K loops go out four MMAs per asm block (one 64-wide plane of the
         // swizzled operands each): fewer instructions between MMAs lets the
         // single issuing thread keep closer to the tensor pipe.
@@ -385,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kq = 0; kq < BN / 64; ++kq)   // 64 keys (4 MMAs of 16) per block
                 umma_bf16_tmem_a_k64(tmem + o_col(t), tmem + s_col(t) + kq * 32,
-                                     dv + ((vo + kq * 4 * 2048) >> 4), kIdescPV, 2048 >> 4,
+                                     dv + ((vo + kq * kVChunk) >> 4), kIdescPV, kVS1 >> 4, kVS2 >> 4,
                                      (!first || kq > 0) ? 1u : 0u);
         };
         auto commit = [&](uint64_t *bar) { umma_commit(bar); };
@@ -483,50 +506,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile's max exceeds it by more than 8, and then (rarely) the row
                 // moves its max, rescales O and redoes the tile from S, which is
                 // intact in TMEM until P is stored over it
+                // S in two halves of 64 keys: the second half's TMEM load is in
+                // flight while the first half's P is computed and stored (over S
+                // columns 0..31, keys 0..31, which stay in registers for a redo)
                 uint32_t pk[BN / 2];
-                float lsum;
-                for (;;) {
-                    uint32_t sr[BN / 32][32];
+                uint32_t sr[BN / 32][32];
+                float lsum, m_tile;
+                const float2 sl2x2 = make_float2(sl2, sl2);
+                auto mask = [&](int c) {
+                    const int lim = pos - key0;
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_addr + s_col(t) + 32 * c, sr[c]);
-                    tmem_wait_ld();
-                    if (diag) {
-                        const int lim = pos - key0;
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * c + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
+                };
+                // key pairs u0..u1-1: P with the max m, their sums and maxima; the
+                // exponent's FMA and the sums as packed fp32 pairs
+                float2 ls;
+                float mx0, mx1;
+                auto pass = [&](auto u0c, auto u1c) {
+                    constexpr int u0 = decltype(u0c)::value, u1 = decltype(u1c)::value;
+                    const float2 negm = make_float2(-m, -m);
 #pragma unroll
-                        for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (32 * c + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
-                    }
-                    if (j == 0 && m == -INFINITY) {
-                        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                        for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                            for (int e = 0; e < 32; e += 4) {
-                                mx0 = fmax3(mx0, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-                                mx1 = fmax3(mx1, __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
-                            }
-                        const float m0 = fmaxf(mx0, mx1) * sl2;
-                        m = m0 == -INFINITY ? 0.f : m0;
-                    }
-                    float ls0 = 0.f, ls1 = 0.f, mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                    for (int u = 0; u < BN / 2; ++u) {
+                    for (int u = u0; u < u1; ++u) {
                         const float s0 = __uint_as_float(sr[u >> 4][(2 * u) & 31]);
                         const float s1 = __uint_as_float(sr[u >> 4][(2 * u + 1) & 31]);
                         if (u & 1) mx1 = fmax3(mx1, s0, s1);
                         else mx0 = fmax3(mx0, s0, s1);
-                        const float p0 = fast_exp2(fmaf(s0, sl2, -m));
-                        const float p1 = fast_exp2(fmaf(s1, sl2, -m));
-                        ls0 += p0;
-                        ls1 += p1;
+                        const float2 x = fma_f32x2(make_float2(s0, s1), sl2x2, negm);
+                        const float p0 = fast_exp2(x.x);
+                        const float p1 = fast_exp2(x.y);
+                        ls = add_f32x2(ls, make_float2(p0, p1));
                         pk[u] = pack_bf16x2(p0, p1);
                     }
-                    lsum = ls0 + ls1;
-                    const float m_tile = fmaxf(mx0, mx1) * sl2;
-                    const bool need = m_tile > m + 8.f;
-                    if (!__any_sync(kFull, need)) break;
+                };
+                using H0 = std::integral_constant<int, 0>;
+                using H1 = std::integral_constant<int, BN / 4>;
+                using H2 = std::integral_constant<int, BN / 2>;
+                tmem_ld32(lane_addr + s_col(t), sr[0]);
+                tmem_ld32(lane_addr + s_col(t) + 32, sr[1]);
+                tmem_wait_ld();
+                tmem_ld32(lane_addr + s_col(t) + 64, sr[2]);
+                tmem_ld32(lane_addr + s_col(t) + 96, sr[3]);
+                if (diag) { mask(0); mask(1); }
+                bool hi_ready = false;
+                if (j == 0 && m == -INFINITY) {
+                    // first tile of the item: its own max, over all keys
+                    tmem_wait_ld_regs(sr[2], sr[3]);
+                    hi_ready = true;
+                    if (diag) { mask(2); mask(3); }
+                    float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            a0 = fmax3(a0, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                            a1 = fmax3(a1, __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
+                        }
+                    const float m0 = fmaxf(a0, a1) * sl2;
+                    m = m0 == -INFINITY ? 0.f : m0;
+                }
+                ls = make_float2(0.f, 0.f);
+                mx0 = -INFINITY;
+                mx1 = -INFINITY;
+                pass(H0{}, H1{});
+                tmem_st32(lane_addr + s_col(t), *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                if (!hi_ready) {
+                    tmem_wait_ld_regs(sr[2], sr[3]);
+                    if (diag) { mask(2); mask(3); }
+                }
+                pass(H1{}, H2{});
+                lsum = ls.x + ls.y;
+                m_tile = fmaxf(mx0, mx1) * sl2;
+                // the tile's max exceeds the running max by more than 8 (rare): move
+                // the max, rescale O and redo the tile from the registers
+                const bool need = m_tile > m + 8.f;
+                if (__any_sync(kFull, need)) {
                     const float m_new = need ? m_tile : m;
                     const float alpha = fast_exp2(m - m_new);
                     l *= alpha;
@@ -541,11 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(lane_addr + o_col(t) + 32 * c, o);
                     }
                     m = m_new;
+                    ls = make_float2(0.f, 0.f);
+                    mx0 = -INFINITY;
+                    mx1 = -INFINITY;
+                    pass(H0{}, H2{});
+                    lsum = ls.x + ls.y;
+                    tmem_wait_st();
+                    tmem_st32(lane_addr + s_col(t), *reinterpret_cast<const uint32_t(*)[32]>(pk));
                 }
-                // P_t over the first BN/2 columns of S_t
-#pragma unroll
-                for (int c = 0; c < BN / 64; ++c)
-                    tmem_st32(lane_addr + s_col(t) + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * c));
+                // the second half of P_t over S columns 32..63
+                tmem_st32(lane_addr + s_col(t) + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
                 l += lsum;
                 // value rows past the context end inside the last block -> zero
                 // (warpgroup 0 only; its p_full arrival orders the writes before
@@ -562,8 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int dh = u / (rows_zero * 8);
                             const int rem = u - dh * rows_zero * 8;
                             const int tok = t_tail + (rem >> 3);
-                            *reinterpret_cast<uint4 *>(vs + dh * kPlaneKV + (bb * kB + tok) * 128 + (rem & 7) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                            const int off = bb * kVBlockBytes + dh * (kB * 128) + tok * 128;
+                            *reinterpret_cast<uint4 *>(vs + off + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                         }
                         fence_proxy_async_smem();
                     }
@@ -631,16 +690,18 @@ CUresult make_q_map(CUtensorMap *map, const void *q, int total_q, int num_heads,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-CUresult make_kv_map(CUtensorMap *map, const void *pool, int num_blocks, int kB, int hkv, int D) {
+CUresult make_kv_map(CUtensorMap *map, const void *pool, int num_blocks, int kB, int hkv, int D,
+                     bool all_planes) {
     auto encode = tensor_map_encoder();
     if (!encode) return CUDA_ERROR_NOT_FOUND;
-    // dims: d_lo(64), token(16), d_hi(D/64), head(Hkv), block; box: one block,
-    // one head, one 64-column plane -> 16 rows of 128 bytes
+    // dims: d_lo(64), token(B), d_hi(D/64), head(Hkv), block; box: one block,
+    // one head, one 64-column plane (B rows of 128 bytes) or all D/64 planes
+    // ([plane][B rows][64] in shared memory)
     const cuuint64_t dims[5] = {64, (cuuint64_t)kB, (cuuint64_t)(D / 64), (cuuint64_t)hkv,
                                 (cuuint64_t)num_blocks};
     const cuuint64_t strides[4] = {(cuuint64_t)hkv * D * 2, 128, (cuuint64_t)D * 2,
                                    (cuuint64_t)kB * hkv * D * 2};
-    const cuuint32_t box[5] = {64, (cuuint32_t)kB, 1, 1, 1};
+    const cuuint32_t box[5] = {64, (cuuint32_t)kB, all_planes ? (cuuint32_t)(D / 64) : 1u, 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -715,8 +776,8 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
 
     CUtensorMap mq, mk, mv;
     if (make_q_map(&mq, a.q, a.total_q, a.num_heads, a.head_dim, pos, G) != CUDA_SUCCESS ||
-        make_kv_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS ||
-        make_kv_map(&mv, a.v_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim) != CUDA_SUCCESS)
+        make_kv_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, false) != CUDA_SUCCESS ||
+        make_kv_map(&mv, a.v_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, true) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
 
     if (!planned) {

@@ -60,6 +60,24 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
     return old;
 }
 
+// Packed fp32 pairs (sm_100 and later): two lanes per instruction, each lane
+// rounded exactly like its scalar form (fmaf, +).
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)),
+          "l"(*reinterpret_cast<const uint64_t *>(&c)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 // max of three (NaN operands are ignored, as for fmaxf)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
@@ -252,21 +270,25 @@ __device__ __forceinline__ void umma_bf16_k64(uint32_t d_tmem, uint64_t a_desc, 
 // Four chained MMAs with the A operand read from tensor memory, over K = 64:
 // A has its M rows on the TMEM lanes and K along the columns, two bf16 per
 // 32-bit column (lower K index in bits 0..15), a_tmem the column of the first
-// K element (lane field 0).  Step k reads A 8 columns (16 K values) further
-// and B `b_step` (16-byte units) further.
+// K element (lane field 0).  Step k reads A 8 columns (16 K values) further;
+// B starts at offsets 0, s1, s2 and s2 + s1 (16-byte units) from b_desc for
+// steps 0..3 (s2 = 2 s1: evenly spaced).
 __device__ __forceinline__ void umma_bf16_tmem_a_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                     uint32_t idesc, uint32_t b_step, uint32_t accumulate) {
+                                                     uint32_t idesc, uint32_t s1, uint32_t s2,
+                                                     uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .b64 b, bs;\n\t.reg .b32 a;\n\t.reg .pred p0, e;\n\t"
-        "setp.ne.b32 p0, %5, 0;\n\tcvt.u64.u32 bs, %4;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "{\n\t.reg .b64 b, b1, b2, b3, x1, x2;\n\t.reg .b32 a;\n\t.reg .pred p0, e;\n\t"
+        "setp.ne.b32 p0, %6, 0;\n\tcvt.u64.u32 x1, %4;\n\tcvt.u64.u32 x2, %5;\n\t"
+        "add.s64 b1, %2, x1;\n\tadd.s64 b2, %2, x2;\n\tadd.s64 b3, b2, x1;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
-        "add.s32 a, %1, 8;\n\tadd.s64 b, %2, bs;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.s32 a, a, 8;\n\tadd.s64 b, b, bs;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.s32 a, a, 8;\n\tadd.s64 b, b, bs;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(b_step), "r"(accumulate));
+        "add.s32 a, %1, 8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b1, %3, 1;\n\t"
+        "add.s32 a, a, 8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b2, %3, 1;\n\t"
+        "add.s32 a, a, 8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b3, %3, 1;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(s1), "r"(s2), "r"(accumulate));
 }
 
 // Arrives once on `bar` when every tcgen05 operation the issuing lane issued
@@ -297,6 +319,23 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Marks the 32 registers of a tcgen05.ld as written here: placed after the
+// tcgen05.wait::ld that completes the load, it keeps every use of them below
+// the wait.
+__device__ __forceinline__ void reg_fence32(uint32_t (&a)[32]) {
+    asm volatile(""
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+                 "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
+                 "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]),
+                 "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]),
+                 "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]));
+}
+// tcgen05.wait::ld for loads into the register arrays a and b.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&a)[32], uint32_t (&b)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    reg_fence32(a);
+    reg_fence32(b);
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive 32-bit columns of this thread's TMEM lane (warp w of a
