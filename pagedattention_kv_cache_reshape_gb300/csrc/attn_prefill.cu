@@ -192,12 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *s_full = kv_empty + kSlots;          // [tile]: S_t written
     uint64_t *p_full = s_full + kMT;               // [tile]: P_t written (and O_t rescaled)
     uint64_t *o_full = p_full + kMT;               // [tile]: last product of the item into O_t done
-    uint64_t *item_full = o_full + kMT;            // [kItemSlots]: item published
+    uint64_t *p_half = o_full + kMT;               // [tile]: P_t's first 64 keys written (and O_t rescaled)
+    uint64_t *item_full = p_half + kMT;            // [kItemSlots]: item published
     uint64_t *item_empty = item_full + kItemSlots; // [kItemSlots]: item read by every consumer
     uint64_t *drained = item_empty + kItemSlots;   // every product issued has completed
     uint32_t &tmem_base_s = *reinterpret_cast<uint32_t *>(drained + 1);
     Item *items = reinterpret_cast<Item *>(drained + 2);       // [kItemSlots]
-    static_assert((3 + 2 * kSlots + 3 * kMT + 2 * kItemSlots) * 8 + kItemSlots * sizeof(Item) <= SH::kBarBytes,
+    static_assert((3 + 2 * kSlots + 4 * kMT + 2 * kItemSlots) * 8 + kItemSlots * sizeof(Item) <= SH::kBarBytes,
                   "barrier area");
 
     // the warp index broadcast from lane 0 is provably warp-uniform, so each
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(s_full + t, 1);
             mbar_init(p_full + t, BM);
             mbar_init(o_full + t, 1);
+            mbar_init(p_half + t, BM);
         }
         for (int i = 0; i < kItemSlots; ++i) {
             mbar_init(item_full + i, 1);
@@ -403,14 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_bf16_k64(tmem + s_col(t), dq + ((uint32_t)(t * kQBytes + pl * kPlaneQ) >> 4),
                               dk + ((ko + pl * kPlaneKV) >> 4), kIdescQK, pl > 0 ? 1u : 0u);
         };
-        auto issue_pv = [&](int t, int nv, bool first) {   // O_t (+)= P_t V, V in ring entry nv
+        // O_t (+)= P_t V over keys 64 kq .. 64 kq + 63 (4 MMAs of 16), V in ring entry nv
+        auto issue_pv = [&](int t, int nv, int kq, bool first) {
             const uint32_t vo = (uint32_t)slot_of(nv) * kSlotBytes;
-#pragma unroll
-            for (int kq = 0; kq < BN / 64; ++kq)   // 64 keys (4 MMAs of 16) per block
-                umma_bf16_tmem_a_k64(tmem + o_col(t), tmem + s_col(t) + kq * 32,
-                                     dv + ((vo + kq * kVChunk) >> 4), kIdescPV, kVS1 >> 4, kVS2 >> 4,
-                                     (!first || kq > 0) ? 1u : 0u);
+            umma_bf16_tmem_a_k64(tmem + o_col(t), tmem + s_col(t) + kq * 32,
+                                 dv + ((vo + kq * kVChunk) >> 4), kIdescPV, kVS1 >> 4, kVS2 >> 4,
+                                 (!first || kq > 0) ? 1u : 0u);
         };
+        static_assert(BN == 128, "P is released in two halves of 64 keys");
         auto commit = [&](uint64_t *bar) { umma_commit(bar); };
         bool ok = true, stopped = false;
         int n = 0, J = 0, nq = 0;
@@ -440,9 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.stall == PA_STALL_CONSUMER && nv >= p.stall_after) { stopped = true; ok = false; break; }
                 if (!mbar_wait_warp(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
                 for (int t = 0; t < kMT; ++t) {
+                    // the first half of P_t goes to the tensor pipe while the
+                    // softmax warpgroup still computes the second
+                    if (!mbar_wait_warp(p_half + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, nv, 0, j == 0);
                     if (!mbar_wait_warp(p_full + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv(t, nv, j == 0);
+                    issue_pv(t, nv, 1, j == 0);
                     if (next) {
                         if (t == 0 && !mbar_wait_warp(kv_full + slot_of(nk), phase_of(nk), p.wait_ns)) { ok = false; break; }
                         tc_fence_after();
@@ -506,108 +513,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile's max exceeds it by more than 8, and then (rarely) the row
                 // moves its max, rescales O and redoes the tile from S, which is
                 // intact in TMEM until P is stored over it
-                // S in two halves of 64 keys: the second half's TMEM load is in
-                // flight while the first half's P is computed and stored (over S
-                // columns 0..31, keys 0..31, which stay in registers for a redo)
-                uint32_t pk[BN / 2];
+                // S is read whole and its max taken first, so P can go out in two
+                // halves of 64 keys (the tensor pipe takes the first while the
+                // second is computed); a later tile runs with the running max m:
+                // P stays <= 2^8 unless the tile's max exceeds it by more than 8,
+                // and then (rarely) the row moves its max and rescales O first
                 uint32_t sr[BN / 32][32];
-                float lsum, m_tile;
-                const float2 sl2x2 = make_float2(sl2, sl2);
                 auto mask = [&](int c) {
                     const int lim = pos - key0;
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         if (32 * c + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
                 };
-                // key pairs u0..u1-1: P with the max m, their sums and maxima; the
-                // exponent's FMA and the sums as packed fp32 pairs
-                float2 ls;
-                float mx0, mx1;
-                auto pass = [&](auto u0c, auto u1c) {
-                    constexpr int u0 = decltype(u0c)::value, u1 = decltype(u1c)::value;
-                    const float2 negm = make_float2(-m, -m);
-#pragma unroll
-                    for (int u = u0; u < u1; ++u) {
-                        const float s0 = __uint_as_float(sr[u >> 4][(2 * u) & 31]);
-                        const float s1 = __uint_as_float(sr[u >> 4][(2 * u + 1) & 31]);
-                        if (u & 1) mx1 = fmax3(mx1, s0, s1);
-                        else mx0 = fmax3(mx0, s0, s1);
-                        const float2 x = fma_f32x2(make_float2(s0, s1), sl2x2, negm);
-                        const float p0 = fast_exp2(x.x);
-                        const float p1 = fast_exp2(x.y);
-                        ls = add_f32x2(ls, make_float2(p0, p1));
-                        pk[u] = pack_bf16x2(p0, p1);
-                    }
-                };
-                using H0 = std::integral_constant<int, 0>;
-                using H1 = std::integral_constant<int, BN / 4>;
-                using H2 = std::integral_constant<int, BN / 2>;
                 tmem_ld32(lane_addr + s_col(t), sr[0]);
                 tmem_ld32(lane_addr + s_col(t) + 32, sr[1]);
                 tmem_wait_ld();
                 tmem_ld32(lane_addr + s_col(t) + 64, sr[2]);
                 tmem_ld32(lane_addr + s_col(t) + 96, sr[3]);
                 if (diag) { mask(0); mask(1); }
-                bool hi_ready = false;
-                if (j == 0 && m == -INFINITY) {
-                    // first tile of the item: its own max, over all keys
-                    tmem_wait_ld_regs(sr[2], sr[3]);
-                    hi_ready = true;
-                    if (diag) { mask(2); mask(3); }
-                    float a0 = -INFINITY, a1 = -INFINITY;
+                float a0 = -INFINITY, a1 = -INFINITY;
+                auto max_of = [&](int c) {
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            a0 = fmax3(a0, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-                            a1 = fmax3(a1, __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
-                        }
-                    const float m0 = fmaxf(a0, a1) * sl2;
-                    m = m0 == -INFINITY ? 0.f : m0;
-                }
-                ls = make_float2(0.f, 0.f);
-                mx0 = -INFINITY;
-                mx1 = -INFINITY;
-                pass(H0{}, H1{});
-                tmem_st32(lane_addr + s_col(t), *reinterpret_cast<const uint32_t(*)[32]>(pk));
-                if (!hi_ready) {
-                    tmem_wait_ld_regs(sr[2], sr[3]);
-                    if (diag) { mask(2); mask(3); }
-                }
-                pass(H1{}, H2{});
-                lsum = ls.x + ls.y;
-                m_tile = fmaxf(mx0, mx1) * sl2;
-                // the tile's max exceeds the running max by more than 8 (rare): move
-                // the max, rescale O and redo the tile from the registers
-                const bool need = m_tile > m + 8.f;
-                if (__any_sync(kFull, need)) {
-                    const float m_new = need ? m_tile : m;
-                    const float alpha = fast_exp2(m - m_new);
-                    l *= alpha;
-                    // PV_t(j-1) completed before S_t(j) was committed, so O_t is final here
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(lane_addr + o_col(t) + 32 * c, o);
+                    for (int e = 0; e < 32; e += 4) {
+                        a0 = fmax3(a0, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                        a1 = fmax3(a1, __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
                     }
-                    m = m_new;
-                    ls = make_float2(0.f, 0.f);
-                    mx0 = -INFINITY;
-                    mx1 = -INFINITY;
-                    pass(H0{}, H2{});
-                    lsum = ls.x + ls.y;
-                    tmem_wait_st();
-                    tmem_st32(lane_addr + s_col(t), *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                };
+                max_of(0);
+                max_of(1);
+                tmem_wait_ld_regs(sr[2], sr[3]);
+                if (diag) { mask(2); mask(3); }
+                max_of(2);
+                max_of(3);
+                const float m_tile = fmaxf(a0, a1) * sl2;
+                if (j == 0 && m == -INFINITY) {
+                    m = m_tile == -INFINITY ? 0.f : m_tile;   // the item's first tile: its own max
+                } else {
+                    const bool need = m_tile > m + 8.f;
+                    if (__any_sync(kFull, need)) {
+                        const float m_new = need ? m_tile : m;
+                        const float alpha = fast_exp2(m - m_new);
+                        l *= alpha;
+                        // PV_t(j-1) completed before S_t(j) was committed, so O_t is final here
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(lane_addr + o_col(t) + 32 * c, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(lane_addr + o_col(t) + 32 * c, o);
+                        }
+                        m = m_new;
+                    }
                 }
-                // the second half of P_t over S columns 32..63
-                tmem_st32(lane_addr + s_col(t) + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
-                l += lsum;
+                // P = 2^(S * scale*log2e - m) for key pairs u0..u0+31 into pk; the
+                // exponent's FMA and the sums as packed fp32 pairs
+                const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m, -m);
+                float2 ls = make_float2(0.f, 0.f);
+                uint32_t pk[BN / 4];
+                auto pass = [&](auto u0c) {
+                    constexpr int u0 = decltype(u0c)::value;
+#pragma unroll
+                    for (int u = u0; u < u0 + BN / 4; ++u) {
+                        const float s0 = __uint_as_float(sr[u >> 4][(2 * u) & 31]);
+                        const float s1 = __uint_as_float(sr[u >> 4][(2 * u + 1) & 31]);
+                        const float2 x = fma_f32x2(make_float2(s0, s1), sl2x2, negm);
+                        const float p0 = fast_exp2(x.x);
+                        const float p1 = fast_exp2(x.y);
+                        ls = add_f32x2(ls, make_float2(p0, p1));
+                        pk[u - u0] = pack_bf16x2(p0, p1);
+                    }
+                };
+                pass(std::integral_constant<int, 0>{});
+                tmem_st32(lane_addr + s_col(t), pk);
                 // value rows past the context end inside the last block -> zero
-                // (warpgroup 0 only; its p_full arrival orders the writes before
+                // (warpgroup 0 only; its p_half arrival orders the writes before
                 // every product that reads this V tile)
                 if (t == 0 && t_tail != 0) {
                     const int bb = lb_last - j * kBlocksPerTile;
@@ -627,6 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fence_proxy_async_smem();
                     }
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_half + t);
+                // the second half of P_t over S columns 32..63
+                pass(std::integral_constant<int, BN / 4>{});
+                tmem_st32(lane_addr + s_col(t) + 32, pk);
+                l += ls.x + ls.y;
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(p_full + t);
