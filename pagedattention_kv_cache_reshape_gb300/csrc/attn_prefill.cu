@@ -46,14 +46,17 @@ constexpr int BN = 128;               // keys per KV tile (8 cache blocks)
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kProducerWarp = 4 * kMT;
 constexpr int kMmaWarp = kProducerWarp + 1;
-constexpr int kThreads = 32 * (4 * kMT + 4);  // the producer and MMA warps fill a warpgroup of their own
-// Register split: launched at 168 a thread (384 x 168 <= 64K), the producer /
-// MMA warpgroup drops to kRegsSide and the softmax warpgroups rise to
-// kRegsSoftmax; 128 * kRegsSide + 256 * kRegsSoftmax <= 384 * 168.
-constexpr int kRegsLaunch = 168;
-constexpr int kRegsSide = 64;
-constexpr int kRegsSoftmax = 216;
-static_assert(128 * kRegsSide + 128 * kMT * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+constexpr int kOutWarp = kProducerWarp + 4;       // first warp of the output warpgroup
+// warpgroups: the softmax ones, the producer / MMA one (two warps idle), the output one
+constexpr int kThreads = 32 * (4 * kMT + 8);
+// Register split: launched at 128 a thread (512 x 128 = 64K), the producer /
+// MMA and the output warpgroups drop to kRegsSide and kRegsOut and the
+// softmax warpgroups rise to kRegsSoftmax, within the launch's total.
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsSide = 56;
+constexpr int kRegsOut = 56;
+constexpr int kRegsSoftmax = 200;
+static_assert(128 * (kRegsSide + kRegsOut) + 128 * kMT * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr int kPlanThreads = 512;
 constexpr int kTmemCols = 512;
 
@@ -109,7 +112,7 @@ template <int D> struct Shape {
     static constexpr int kSlotBytes = BN * D * 2;      // K or V of one KV tile
     static constexpr int kPlaneQ = BM * 128;           // one 64-column plane of Q
     static constexpr int kPlaneKV = BN * 128;          // one 64-column plane of K or V
-    static constexpr int kBarBytes = 512;      // barriers, TMEM address, item slots
+    static constexpr int kBarBytes = 2816;     // barriers, TMEM address, item slots, row sums
     static constexpr int kFit = (int)((kSmemLimit - kMT * kQBytes - kBarBytes) / kSlotBytes);
     static constexpr int kSlots = kFit < 8 ? kFit : 8;  // K/V ring depth
     static constexpr size_t kSmem = (size_t)kMT * kQBytes + (size_t)kSlots * kSlotBytes + kBarBytes;
@@ -193,12 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_full + kMT;               // [tile]: P_t written (and O_t rescaled)
     uint64_t *o_full = p_full + kMT;               // [tile]: last product of the item into O_t done
     uint64_t *p_half = o_full + kMT;               // [tile]: P_t's first 64 keys written (and O_t rescaled)
-    uint64_t *item_full = p_half + kMT;            // [kItemSlots]: item published
+    uint64_t *o_empty = p_half + kMT;              // [tile]: O_t read by the output warpgroup
+    uint64_t *l_full = o_empty + kMT;              // [tile]: the item's row sums of tile t written
+    uint64_t *item_full = l_full + kMT;            // [kItemSlots]: item published
     uint64_t *item_empty = item_full + kItemSlots; // [kItemSlots]: item read by every consumer
     uint64_t *drained = item_empty + kItemSlots;   // every product issued has completed
     uint32_t &tmem_base_s = *reinterpret_cast<uint32_t *>(drained + 1);
     Item *items = reinterpret_cast<Item *>(drained + 2);       // [kItemSlots]
-    static_assert((3 + 2 * kSlots + 4 * kMT + 2 * kItemSlots) * 8 + kItemSlots * sizeof(Item) <= SH::kBarBytes,
+    float *l_s = reinterpret_cast<float *>(items + kItemSlots);   // [item parity][tile][row]: row sums
+    static_assert((3 + 2 * kSlots + 6 * kMT + 2 * kItemSlots) * 8 + kItemSlots * sizeof(Item) +
+                          2 * kMT * BM * sizeof(float) <= SH::kBarBytes,
                   "barrier area");
 
     // the warp index broadcast from lane 0 is provably warp-uniform, so each
@@ -224,10 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(p_full + t, BM);
             mbar_init(o_full + t, 1);
             mbar_init(p_half + t, BM);
+            mbar_init(o_empty + t, BM);
+            mbar_init(l_full + t, BM);
         }
         for (int i = 0; i < kItemSlots; ++i) {
             mbar_init(item_full + i, 1);
-            mbar_init(item_empty + i, 1 + 4 * kMT);      // the MMA warp and every softmax warp
+            mbar_init(item_empty + i, 1 + 4 * kMT + 4);  // the MMA warp, every softmax and output warp
         }
         mbar_init(drained, 1);
         fence_mbar_init();
@@ -262,7 +271,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
     };
 
-    if (warp >= kProducerWarp) {
+    if (warp >= kOutWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOut));
+        // ================= output warpgroup: thread r writes row r of M-tile t
+        // as O_t / l, after the item's last product into O_t; the MMA warp
+        // waits for its o_empty before the next item's first product into O_t
+        const int r = tid & (BM - 1);
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        bool ok = true;
+        int no = 0;
+        for (int it = 0; ok; ++it) {
+            Item I;
+            if (!take_item(it, I)) { ok = false; break; }
+            if (!I.live) break;
+            if (!I.valid) continue;
+            for (int t = 0; t < kMT; ++t) {
+                if (!mbar_wait_warp(o_full + t, (uint32_t)(no & 1), p.wait_ns) ||
+                    !mbar_wait_warp(l_full + t, (uint32_t)(no & 1), p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float inv = 1.f / l_s[((no & 1) * kMT + t) * BM + r];
+                const int i = t * POS + (r & (POS - 1));    // position index within the CTA tile
+                const bool row_valid = i < I.nrows_all;
+                __nv_bfloat16 *dst = p.out + ((int64_t)(I.q0 + I.i0 + (row_valid ? i : 0)) * p.num_heads +
+                                              (int64_t)I.g * p.group + (r >> p.pos_shift)) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o0[16], o1[16];
+                    tmem_ld16(lane_addr + o_col(t) + 32 * c, o0);
+                    tmem_ld16(lane_addr + o_col(t) + 32 * c + 16, o1);
+                    tmem_wait_ld();
+                    if (c == D / 32 - 1) {       // O_t read: the next item's products may overwrite it
+                        tc_fence_before();
+                        mbar_arrive(o_empty + t);
+                    }
+                    if (row_valid) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t *v = h ? o1 : o0;
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                const uint32_t *v8 = v + 8 * q;
+                                uint4 w;
+                                w.x = pack_bf16x2(__uint_as_float(v8[0]) * inv, __uint_as_float(v8[1]) * inv);
+                                w.y = pack_bf16x2(__uint_as_float(v8[2]) * inv, __uint_as_float(v8[3]) * inv);
+                                w.z = pack_bf16x2(__uint_as_float(v8[4]) * inv, __uint_as_float(v8[5]) * inv);
+                                w.w = pack_bf16x2(__uint_as_float(v8[6]) * inv, __uint_as_float(v8[7]) * inv);
+                                *reinterpret_cast<uint4 *>(dst + 32 * c + 16 * h + 8 * q) = w;
+                            }
+                        }
+                    }
+                }
+            }
+            if (!ok) break;
+            ++no;
+        }
+        if (!ok && r == 0) {
+            set_status(p.status, PA_ERR_TIMEOUT);
+            note_wait_site(p.wait_sites, PA_WAIT_PREFILL_SOFTMAX);
+        }
+    } else if (warp >= kProducerWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSide));
     if (warp == kProducerWarp) {
         // ================= TMA producer
@@ -442,6 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.stall == PA_STALL_CONSUMER && nv >= p.stall_after) { stopped = true; ok = false; break; }
                 if (!mbar_wait_warp(kv_full + slot_of(nv), phase_of(nv), p.wait_ns)) { ok = false; break; }
                 for (int t = 0; t < kMT; ++t) {
+                    // the item's first product into O_t overwrites it: the output
+                    // warpgroup has read the previous item's O_t
+                    if (j == 0 && nq > 0 && !mbar_wait_warp(o_empty + t, (uint32_t)((nq - 1) & 1), p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
                     // the first half of P_t goes to the tensor pipe while the
                     // softmax warpgroup still computes the second
                     if (!mbar_wait_warp(p_half + t, (uint32_t)((J + j) & 1), p.wait_ns)) { ok = false; break; }
@@ -484,7 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= softmax warpgroup t: thread r owns row r of M-tile t
         const int t = warp >> 2;
         const int r = tid & (BM - 1);
-        const int h_local = r >> p.pos_shift;
         const int i = t * POS + (r & (POS - 1));          // position index within the CTA tile
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float sl2 = p.scale_log2;
@@ -620,32 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(p_full + t);
             }
             if (!ok) break;
-            // ---- epilogue: O / l -> bf16 rows of out, after the last product into O_t.
-            // The next item's first product into O_t waits for this warpgroup's
-            // next P, so these TMEM loads complete before O_t is overwritten.
-            if (!mbar_wait_warp(o_full + t, (uint32_t)(no & 1), p.wait_ns)) { ok = false; break; }
-            tc_fence_after();
-            const float inv = 1.f / l;
-            __nv_bfloat16 *dst = p.out + ((int64_t)(I.q0 + I.i0 + i) * p.num_heads +
-                                          (int64_t)I.g * p.group + h_local) * D;
-            uint32_t o[D / 32][32];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_addr + o_col(t) + 32 * c, o[c]);
-            tmem_wait_ld();
-            if (row_valid) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint32_t *v8 = o[c] + 8 * q4;
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(v8[0]) * inv, __uint_as_float(v8[1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(v8[2]) * inv, __uint_as_float(v8[3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(v8[4]) * inv, __uint_as_float(v8[5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(v8[6]) * inv, __uint_as_float(v8[7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = v;
-                    }
-            }
+            // the row's sum for the output warpgroup (double-buffered by item:
+            // this buffer's previous contents, two items back, were read before
+            // the output warpgroup released O_t for the item in between)
+            l_s[((no & 1) * kMT + t) * BM + r] = l;
+            mbar_arrive(l_full + t);
             n += 2 * I.nkv;
             J += I.nkv;
             ++no;
