@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool row_valid = i < I.nrows_all;
                 __nv_bfloat16 *dst = p.out + ((int64_t)(I.q0 + I.i0 + (row_valid ? i : 0)) * p.num_heads +
                                               (int64_t)I.g * p.group + (r >> p.pos_shift)) * D;
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o0[16], o1[16];
                     tmem_ld16(lane_addr + o_col(t) + 32 * c, o0);
@@ -308,19 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(o_empty + t);
                     }
                     if (row_valid) {
+                        // 32-byte stores: whole sectors of the row
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const uint32_t *v = h ? o1 : o0;
+                            uint32_t w[8];
 #pragma unroll
-                            for (int q = 0; q < 2; ++q) {
-                                const uint32_t *v8 = v + 8 * q;
-                                uint4 w;
-                                w.x = pack_bf16x2(__uint_as_float(v8[0]) * inv, __uint_as_float(v8[1]) * inv);
-                                w.y = pack_bf16x2(__uint_as_float(v8[2]) * inv, __uint_as_float(v8[3]) * inv);
-                                w.z = pack_bf16x2(__uint_as_float(v8[4]) * inv, __uint_as_float(v8[5]) * inv);
-                                w.w = pack_bf16x2(__uint_as_float(v8[6]) * inv, __uint_as_float(v8[7]) * inv);
-                                *reinterpret_cast<uint4 *>(dst + 32 * c + 16 * h + 8 * q) = w;
-                            }
+                            for (int e = 0; e < 8; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+                            st_global_v8(dst + 32 * c + 16 * h, w);
                         }
                     }
                 }

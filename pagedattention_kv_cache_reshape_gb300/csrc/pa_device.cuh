@@ -78,6 +78,13 @@ __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
     return *reinterpret_cast<const float2 *>(&d);
 }
 
+// One 32-byte store (sm_100 and later); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&r)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // max of three (NaN operands are ignored, as for fmaxf)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
