@@ -65,13 +65,14 @@ constexpr int kPartialCtas = 512;   // partial slots reserved for CTA boundaries
 constexpr int kPlanThreads = 256;
 constexpr int kSmemBudget = 227 * 1024;
 // Per-SM rates for splitting the SMs between the decode rows and a concurrent
-// prefill kernel (GB300): the tcgen05 prefill kernel sustains about 5.9
-// TFLOP/s per SM on causal chunks; the decode kernel streams up to about 82
-// GB/s from one SM alone, but beside the prefill kernel (both drawing on DRAM)
-// the split balances best at 64 GB/s per SM: a sweep of 50-88 on the 8 x 512
-// + 248-row mixed batch put the step at its shortest between 58 and 70.
+// prefill kernel (GB300): the tcgen05 prefill kernel sustains about 7.6
+// TFLOP/s per SM on causal chunks alone, but beside the decode kernel the
+// split balances best at 6.6 (a sweep of 5.9-8.2 on the 8 x 512 + 248-row mixed
+// batch); the decode kernel streams up to about 82 GB/s from one SM alone,
+// and the split balances best at 64 GB/s per SM: a sweep of 50-88 put the step
+// at its shortest between 58 and 70.
 constexpr double kDecodeBytesPerSmNs = 64.0;
-constexpr double kPrefillFlopsPerSmNs = 5900.0;
+constexpr double kPrefillFlopsPerSmNs = 6600.0;
 
 struct __align__(16) StreamEntry {
     int32_t seq;
