@@ -166,8 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kDH = SH::kDH, kQBytes = SH::kQBytes, kSlotBytes = SH::kSlotBytes;
     constexpr int kPlaneQ = SH::kPlaneQ, kPlaneKV = SH::kPlaneKV, kSlots = SH::kSlots;
     // V tile layout, block-major: [block][D/64 plane][B rows][64], one TMA box
-    // per block for all planes (K needs one box per block and plane: its
-    // K-major operand wants the 128 keys of a plane at one row pitch).  Key k
+    // per block for all planes.  Key k
     // sits at (k / B) * kVBlockBytes + (k % B) * 128 in a plane; 16-key MMA steps
     // 0..3 of 64 keys start at 0, kVS1, kVS2 and kVS2 + kVS1; their 8-row groups
     // are kVSbo apart and their planes B*128.
@@ -178,6 +177,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kVChunk = 64 / kB * kVBlockBytes;                    // 64 keys
     constexpr int kVLbo = kB * 128;
     constexpr int kVSbo = kB < 16 ? kVBlockBytes : 1024;
+    // K tile layout: plane-major, [D/64 plane][128 keys][64], one box per block and
+    // plane, except at B = 8, where a block is exactly one 8-row group of the
+    // K-major operand: block-major like V, one box per block, the groups of a
+    // plane kVBlockBytes apart and the planes B*128.
+    constexpr bool kKBlockMajor = kB == 8;
+    constexpr int kKSbo = kKBlockMajor ? kVBlockBytes : 1024;
+    constexpr int kKPlane = kKBlockMajor ? kB * 128 : kPlaneKV;
     constexpr uint32_t kIdescQK = umma_idesc_bf16(BM, BN, 0);
     constexpr uint32_t kIdescPV = umma_idesc_bf16(BM, D, 1);
     constexpr uint32_t kFull = 0xffffffffu;
@@ -423,10 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (lane == 0) mbar_arrive_expect_tx(kv_full + slot_of(m), kSlotBytes);
                     __syncwarp();
-                    if (kv) {
+                    if (kv || kKBlockMajor) {
                         if (lane < kBlocksPerTile)
-                            tma_load_5d(kv_s + slot_of(m) * kSlotBytes + lane * kVBlockBytes, &tmap_v, 0, 0, 0, I.g,
-                                        cbv, kv_full + slot_of(m));
+                            tma_load_5d(kv_s + slot_of(m) * kSlotBytes + lane * kVBlockBytes, kv ? &tmap_v : &tmap_k,
+                                        0, 0, 0, I.g, cbv, kv_full + slot_of(m));
                     } else if (lane < kBlocksPerTile * kDH) {
                         tma_load_5d(kv_s + slot_of(m) * kSlotBytes + dh * kPlaneKV + b * (kB * 128),
                                     kv ? &tmap_v : &tmap_k, 0, 0, dh, I.g, cb, kv_full + slot_of(m));
@@ -459,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(kv_s);
         // descriptors: constant fields + (address >> 4) in bits 0..13
         const uint64_t dq = umma_desc_sw128(q_addr, 16, 1024);
-        const uint64_t dk = umma_desc_sw128(kv_addr, 16, 1024);
+        const uint64_t dk = umma_desc_sw128(kv_addr, 16, kKSbo);
         const uint64_t dv = umma_desc_sw128(kv_addr, kVLbo, kVSbo);
         // The K loops go out four MMAs per asm block (one 64-wide plane of the
         // swizzled operands each): fewer instructions between MMAs lets the
@@ -469,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int pl = 0; pl < D / 64; ++pl)
                 umma_bf16_k64(tmem + s_col(t), dq + ((uint32_t)(t * kQBytes + pl * kPlaneQ) >> 4),
-                              dk + ((ko + pl * kPlaneKV) >> 4), kIdescQK, pl > 0 ? 1u : 0u);
+                              dk + ((ko + pl * kKPlane) >> 4), kIdescQK, pl > 0 ? 1u : 0u);
         };
         // O_t (+)= P_t V over keys 64 kq .. 64 kq + 63 (4 MMAs of 16), V in ring entry nv
         auto issue_pv = [&](int t, int nv, int kq, bool first) {
@@ -814,7 +820,8 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
 
     CUtensorMap mq, mk, mv;
     if (make_q_map(&mq, a.q, a.total_q, a.num_heads, a.head_dim, pos, G) != CUDA_SUCCESS ||
-        make_kv_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, false) != CUDA_SUCCESS ||
+        make_kv_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, a.block_size == 8) !=
+            CUDA_SUCCESS ||
         make_kv_map(&mv, a.v_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, true) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
 
