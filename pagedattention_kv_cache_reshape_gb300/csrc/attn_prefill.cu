@@ -13,14 +13,18 @@
 // Work unit (one CTA): two M-tiles of 128 rows; a tile is POS consecutive
 // query positions x the G query heads of one kv-head, so each K/V tile is
 // loaded once for 2*POS positions of the whole group.  Keys come in tiles of
-// 128 (8 cache blocks); K and V of a tile take one slot each of a TMA ring.
+// 128 (16, 8 or 4 cache blocks); K and V of a tile take one slot each of a TMA
+// ring, V block-major (one box per cache block), K plane-major (one box per
+// block and 64-column plane; block-major at B = 8).
 // Warp roles: warps 0-7 two softmax warpgroups (thread = row = TMEM lane of
-// its tile), warp 8 TMA producer, warp 9 TMEM owner and MMA issuer.
+// its tile), warp 8 TMA producer, warp 9 TMEM owner and MMA issuer, warps
+// 12-15 the output warpgroup (O / l to the rows of out).
 //   S_t = Q_t K_j^T                         -> TMEM, fp32 (128 columns per tile)
-//   P_t = exp2(S_t * scale*log2e - m)       -> TMEM over S_t, bf16 pairs
+//   P_t = exp2(S_t * scale*log2e - m)       -> TMEM over S_t, bf16 pairs, in two halves
 //   O_t += P_t V_j                          -> TMEM, fp32; A operand P_t read from TMEM
 // The two M-tiles alternate on the tensor pipe: while one softmax warpgroup
-// turns S into P, the products of the other tile run.
+// turns S into P, the products of the other tile run; the first half of P
+// goes to the tensor pipe while the second is computed.
 // The running max is only raised (and O rescaled in TMEM) when a row's max
 // grows by more than 2^8; otherwise the stale max is kept, which changes no
 // result because l uses the same max.  Causal masking is a select on the
