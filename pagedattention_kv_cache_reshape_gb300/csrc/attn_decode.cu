@@ -14,13 +14,14 @@
 //    groups the virtual stream has NHG*T entries.
 //  * main kernel -- one persistent CTA per SM takes an equal contiguous slice
 //    of the virtual stream, so every CTA reads the same number of cache bytes
-//    whatever the length mix.  A producer warp loads each 16-token block of
+//    whatever the length mix.  A producer warp loads each 16-token unit of
 //    KVH kv-heads (32 KB of K and 32 KB of V for 8 heads x 128 dims) with one
-//    TMA tensor copy each into a ring of shared-memory stages (128-byte
-//    swizzle), plus the sequence's query heads when a new sequence starts.
+//    TMA tensor copy each (two at block size 8) into a ring of shared-memory
+//    stages (128-byte swizzle), plus the sequence's query heads when a new
+//    sequence starts.
 //    A consumer warp owns up to 8 q-heads of one kv-head (a kv-head with G > 8
 //    q-heads gets ceil(G/8) warps): S^T = K Q^T and O^T += V^T P^T run on the
-//    tensor cores (mma m16n8k16, bf16 in, fp32 out), the block's 16 tokens in
+//    tensor cores (mma m16n8k16, bf16 in, fp32 out), the unit's 16 tokens in
 //    M and the q-heads in N, with an online softmax (running max / sum,
 //    base-2 exponent) in fp32.
 //    A sequence slice wholly inside one CTA is normalised and stored.  A
@@ -552,10 +553,10 @@ __device__ __forceinline__ void merge_group(const DecodeParams &p, int64_t slot0
 }
 
 // ------------------------------------------------------------------ early prefetch
-// While the decode CTA waits for the plan, it finds the first blocks of its
+// While the decode CTA waits for the plan, it finds the first units of its
 // own slice from context_lens and the block tables (the same partition the
-// plan builds: the blocks of all sequences in order, cut into P equal slices)
-// and prefetches them into L2, so the first copies after the wait hit L2.  A
+// plan builds: the units of all sequences in order, cut into P equal slices)
+// and prefetches their blocks' rows into L2, so the first copies after the wait hit L2.  A
 // prefetch is only a hint: it reads inputs before the wait, and a stale value
 // would cost time, never a wrong result.  Threads [0, nthr) take part (the
 // consumer warps: the producer goes straight on to its wait and first
@@ -809,7 +810,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     }
 
     // ================= consumer warp w: q-heads [hoff, hoff + gcount) of kv-head kh
-    // Products taken transposed, so that the 16 tokens of a block fill the M
+    // Products taken transposed, so that the 16 tokens of a unit fill the M
     // of m16n8k16 and up to 8 q-heads its N:
     //   S^T (16 tokens x heads) = K Q^T and O^T (D x heads) += V^T P^T.
     // Lane l holds heads 2(l%4) and 2(l%4)+1 (n) of tokens / dims l/4 and
@@ -1211,7 +1212,7 @@ cudaError_t launch_split_decode(const AttnArgs &a, void *workspace, size_t works
     prm.stall_after = wt.after;
     prm.wait_sites = wt.sites;
 
-    // tensor maps: one TMA per block for all kv-heads of the CTA
+    // tensor maps: one TMA per unit (two at B = 8) for all kv-heads of the CTA
     CUtensorMap mk, mv;
     prm.tma_heads = L.kvh;
     if (make_pool_map(&mk, a.k_cache, a.num_blocks, B, a.num_kv_heads, a.head_dim, L.kvh, true) != CUDA_SUCCESS ||
