@@ -152,3 +152,37 @@ def test_block_size_deterministic_and_permutation_invariant(B):
     o3 = pa.decode(w.q, kp, vp, bt, w.context_lens, w.scale)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(o1, o3)
+
+
+def _poison_unused(w):
+    """NaN into every pool slot no sequence reads: unreferenced blocks and the
+    tail of each sequence's last block (live slots found with the oracle)."""
+    wc = w.to("cpu")
+    slots = []
+    for s in range(w.num_seqs):
+        cu = torch.tensor([0, int(wc.context_lens[s])], dtype=torch.int32)
+        slots.append(oracle.slot_mapping(wc.block_tables[s:s + 1], torch.zeros(1, dtype=torch.int32),
+                                         cu, w.block_size, w.num_blocks))
+    live = np.unique(np.concatenate(slots))
+    mask = torch.ones(w.num_blocks * w.block_size, dtype=torch.bool)
+    mask[torch.from_numpy(live)] = False
+    mask = mask.to(DEV)
+    for pool in (w.k_cache, w.v_cache):
+        pool.view(w.num_blocks * w.block_size, -1)[mask] = float("nan")
+
+
+@pytest.mark.parametrize("B", SIZES)
+@pytest.mark.parametrize("name", ["gqa_small", "mixed_small", "prefill_gqa4", "prefill_g16_d64"])
+def test_block_size_nan_poison_in_unused_slots_never_reaches_output(name, B):
+    """The rows past a sequence's end inside its last block, and whole unused
+    blocks, may hold anything: outputs stay finite and bit for bit those of a
+    clean pool (at B = 8 the decode's two-block units and the prefill's
+    block-major K tiles read such rows)."""
+    clean = CASES[name](43, B)
+    _, out_clean = gpu_step(clean)
+    dirty = CASES[name](43, B)
+    _poison_unused(dirty)
+    _, out_dirty = gpu_step(dirty)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out_dirty.float()).all()
+    assert torch.equal(out_clean, out_dirty)
