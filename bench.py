@@ -677,7 +677,8 @@ def measure_configs(args, pa, dev, flush_l2, n):
     """Each of the five workload configurations through the same step and
     timing as the headline: median and mean of n event-timed steps (L2 flushed
     before each), its main attention kernel likewise, and its roofline
-    fraction.  For the mixed step also the prefill chunks alone."""
+    fraction.  For the mixed step also the prefill chunks alone, and the
+    prefill kernel alone at 8 chunks of 512 tokens over 2048 cached ones."""
     peak, _ = measured_peaks()
     tc_peak = measured_tflops()
     out = {}
@@ -725,6 +726,20 @@ def measure_configs(args, pa, dev, flush_l2, n):
         out[name] = e
         del w
         torch.cuda.empty_cache()
+    # the prefill kernel on its own at the mixed step's chunk shape with the
+    # longest cached prefix (8 chunks of 512 new tokens over 2048 cached
+    # tokens): the call is a plan launch and the prefill kernel
+    wp = W.prefill_chunks(args.seed, pa.num_blocks_needed, device=dev)
+    rp = StepRunner(pa, wp, dev, 3, not args.no_graph)
+    pm = rp.time_kernel(n, flush_l2)
+    rp.check_status("in a config's timed region")
+    pf = prefill_flops(wp)
+    pmed = float(np.median(pm))
+    out["prefill8x512_bf16"] = {"steps": n, "kernel": "plan + prefill_kernel", "call_us": stats_us(pm),
+                                "flops": pf, "tflops": round(pf / (pmed / 1e3) / 1e12, 1),
+                                "frac": round(pf / (pmed / 1e3) / 1e12 / tc_peak, 4)}
+    del rp, wp
+    torch.cuda.empty_cache()
     return out
 
 

@@ -14,8 +14,7 @@
 // query positions x the G query heads of one kv-head, so each K/V tile is
 // loaded once for 2*POS positions of the whole group.  Keys come in tiles of
 // 128 (16, 8 or 4 cache blocks); K and V of a tile take one slot each of a TMA
-// ring, V block-major (one box per cache block), K plane-major (one box per
-// block and 64-column plane; block-major at B = 8).
+// ring, both with one box per cache block.
 // Warp roles: warps 0-7 two softmax warpgroups (thread = row = TMEM lane of
 // its tile), warp 8 TMA producer, warp 9 TMEM owner and MMA issuer, warps
 // 12-15 the output warpgroup (O / l to the rows of out).
@@ -115,7 +114,6 @@ template <int D> struct Shape {
     static constexpr int kQBytes = BM * D * 2;         // one M-tile of Q
     static constexpr int kSlotBytes = BN * D * 2;      // K or V of one KV tile
     static constexpr int kPlaneQ = BM * 128;           // one 64-column plane of Q
-    static constexpr int kPlaneKV = BN * 128;          // one 64-column plane of K or V
     static constexpr int kBarBytes = 2816;     // barriers, TMEM address, item slots, row sums
     static constexpr int kFit = (int)((kSmemLimit - kMT * kQBytes - kBarBytes) / kSlotBytes);
     static constexpr int kSlots = kFit < 8 ? kFit : 8;  // K/V ring depth
@@ -165,10 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
     constexpr int kBlocksPerTile = BN / kB;          // cache blocks per KV tile
-    static_assert(kBlocksPerTile * (D / 64) <= 32, "one TMA box per producer lane");
+    static_assert(kBlocksPerTile <= 32, "one TMA box per producer lane");
     using SH = Shape<D>;
     constexpr int kDH = SH::kDH, kQBytes = SH::kQBytes, kSlotBytes = SH::kSlotBytes;
-    constexpr int kPlaneQ = SH::kPlaneQ, kPlaneKV = SH::kPlaneKV, kSlots = SH::kSlots;
+    constexpr int kPlaneQ = SH::kPlaneQ, kSlots = SH::kSlots;
     // V tile layout, block-major: [block][D/64 plane][B rows][64], one TMA box
     // per block for all planes.  Key k
     // sits at (k / B) * kVBlockBytes + (k % B) * 128 in a plane; 16-key MMA steps
@@ -181,13 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kVChunk = 64 / kB * kVBlockBytes;                    // 64 keys
     constexpr int kVLbo = kB * 128;
     constexpr int kVSbo = kB < 16 ? kVBlockBytes : 1024;
-    // K tile layout: plane-major, [D/64 plane][128 keys][64], one box per block and
-    // plane, except at B = 8, where a block is exactly one 8-row group of the
-    // K-major operand: block-major like V, one box per block, the groups of a
-    // plane kVBlockBytes apart and the planes B*128.
-    constexpr bool kKBlockMajor = kB == 8;
-    constexpr int kKSbo = kKBlockMajor ? kVBlockBytes : 1024;
-    constexpr int kKPlane = kKBlockMajor ? kB * 128 : kPlaneKV;
+    // K tile layout, block-major too, one TMA box per block: a block is
+    // [B/8 row group][D/64 plane][8 rows][64], so across the tile the 8-row
+    // groups of one plane sit D/64 * 1024 bytes apart (the K-major operand's
+    // single group stride) and the planes 1024 bytes apart.
+    constexpr int kKSbo = kDH * 1024;
+    constexpr int kKPlane = 1024;
     constexpr uint32_t kIdescQK = umma_idesc_bf16(BM, BN, 0);
     constexpr uint32_t kIdescPV = umma_idesc_bf16(BM, D, 1);
     constexpr uint32_t kFull = 0xffffffffu;
@@ -414,11 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++chunk_cur;
                     ids_next = load_ids(chunk_cur + 1);
                 }
-                // lane (block b, plane dh) copies one box of K (one plane of one
-                // block); V block-major: lane b < kBlocksPerTile copies block b
-                const int b = lane / kDH, dh = lane % kDH;
                 const int id0 = (j * kBlocksPerTile) & 31;
-                const int cb = __shfl_sync(kFull, ids_cur, id0 + (b & (kBlocksPerTile - 1)));
                 const int cbv = __shfl_sync(kFull, ids_cur, id0 + (lane & (kBlocksPerTile - 1)));
                 for (int kv = 0; kv < 2; ++kv) {
                     const int m = n + 2 * j + kv;
@@ -433,13 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (lane == 0) mbar_arrive_expect_tx(kv_full + slot_of(m), kSlotBytes);
                     __syncwarp();
-                    if (kv || kKBlockMajor) {
-                        if (lane < kBlocksPerTile)
-                            tma_load_5d(kv_s + slot_of(m) * kSlotBytes + lane * kVBlockBytes, kv ? &tmap_v : &tmap_k,
-                                        0, 0, 0, I.g, cbv, kv_full + slot_of(m));
-                    } else if (lane < kBlocksPerTile * kDH) {
-                        tma_load_5d(kv_s + slot_of(m) * kSlotBytes + dh * kPlaneKV + b * (kB * 128),
-                                    kv ? &tmap_v : &tmap_k, 0, 0, dh, I.g, cb, kv_full + slot_of(m));
+                    // lane b < kBlocksPerTile copies block b of K or V
+                    if (lane < kBlocksPerTile) {
+                        uint8_t *dst = kv_s + slot_of(m) * kSlotBytes + lane * kVBlockBytes;
+                        if (kv)
+                            tma_load_5d(dst, &tmap_v, 0, 0, 0, I.g, cbv, kv_full + slot_of(m));
+                        else if (kB == 8)
+                            tma_load_5d(dst, &tmap_k, 0, 0, 0, I.g, cbv, kv_full + slot_of(m));
+                        else
+                            tma_load_5d(dst, &tmap_k, 0, 0, I.g * kDH, 0, cbv, kv_full + slot_of(m));
                     }
                     issued_end = m + 1;
                 }
@@ -756,6 +751,24 @@ CUresult make_kv_map(CUtensorMap *map, const void *pool, int num_blocks, int kB,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// K at B = 16 and 32, one box per cache block with every 64-column plane:
+// dims d_lo(64), token within an 8-row group, 64-column quarter of a row
+// (head * D/64 + plane, 128 bytes apart), 8-row group of the block, block.
+// The box lands as [group][plane][8 rows][64].  (At B = 8 a block is one
+// group and make_kv_map's all-planes box gives the same layout.)
+CUresult make_k_map(CUtensorMap *map, const void *pool, int num_blocks, int kB, int hkv, int D) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[5] = {64, 8, (cuuint64_t)hkv * (D / 64), (cuuint64_t)(kB / 8), (cuuint64_t)num_blocks};
+    const cuuint64_t strides[4] = {(cuuint64_t)hkv * D * 2, 128, (cuuint64_t)8 * hkv * D * 2,
+                                   (cuuint64_t)kB * hkv * D * 2};
+    const cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), (cuuint32_t)(kB / 8), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int log2_exact(int v) {
@@ -824,8 +837,9 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, void *workspace, size_t workspa
 
     CUtensorMap mq, mk, mv;
     if (make_q_map(&mq, a.q, a.total_q, a.num_heads, a.head_dim, pos, G) != CUDA_SUCCESS ||
-        make_kv_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, a.block_size == 8) !=
-            CUDA_SUCCESS ||
+        (a.block_size == 8
+             ? make_kv_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, true)
+             : make_k_map(&mk, a.k_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim)) != CUDA_SUCCESS ||
         make_kv_map(&mv, a.v_cache, a.num_blocks, a.block_size, a.num_kv_heads, a.head_dim, true) != CUDA_SUCCESS)
         return cudaErrorNotSupported;
 

@@ -258,9 +258,21 @@ def long_single(seed: int, blocks_needed: BlocksNeeded, device="cpu") -> Workloa
     return long(seed, blocks_needed, num_seqs=1, ctx=131072, num_blocks=10240, device=device)
 
 
+def prefill_chunks(seed: int, blocks_needed: BlocksNeeded, num_seqs: int = 8, chunk: int = 512,
+                   cached: int = 2048, block_size: int = 16, device="cpu") -> Workload:
+    """Prefill alone: num_seqs chunks of `chunk` new tokens, each over `cached`
+    already-cached tokens (the mixed step's chunk shape at its longest prefix),
+    32/8 heads, head_dim 128, bf16."""
+    return build(f"prefill{num_seqs}x{chunk}_bf16", seed=seed, blocks_needed=blocks_needed,
+                 dtype=torch.bfloat16, num_heads=32, num_kv_heads=8, head_dim=128, block_size=block_size,
+                 q_lens=np.full(num_seqs, chunk), context_lens=np.full(num_seqs, cached + chunk),
+                 device=device)
+
+
 # shapes measured beside the five configurations above (not among them)
 EXTRA_CONFIGS = {
     "long1x131k_bf16": long_single,
+    "prefill8x512_bf16": prefill_chunks,
 }
 
 
