@@ -67,3 +67,16 @@ def test_long_config_outliers_are_exact_multiples():
     # scaled rows are x8 of an N(0,1) bf16 row: dividing by 8 is exact in bf16
     scaled = rows[big] / 8
     assert torch.equal(scaled.to(torch.bfloat16).float(), scaled)
+
+
+def test_prefill_chunks_config_structure():
+    # 3 chunks of 40 new tokens over 70 cached ones: every row a prefill row,
+    # each sequence's new tokens at the end of its context
+    w = W.prefill_chunks(0, NB, num_seqs=3, chunk=40, cached=70)
+    assert w.q_lens.tolist() == [40, 40, 40]
+    assert w.context_lens.tolist() == [110, 110, 110]
+    assert not w.decode_only and w.total_q == 120
+    assert (w.seq_start.numpy() == 70).all()
+    assert w.num_heads == 32 and w.num_kv_heads == 8 and w.head_dim == 128 and w.dtype == torch.bfloat16
+    assert w.blocks_per_seq == [NB(110, 16)] * 3
+    assert "prefill8x512_bf16" in W.EXTRA_CONFIGS
