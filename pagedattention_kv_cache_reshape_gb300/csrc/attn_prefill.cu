@@ -370,10 +370,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return okp;
         };
+        // block ids of item X, 32 per chunk (lane l holds block 32*chunk + l);
+        // past the sequence end (or invalid) the coordinate num_blocks is out
+        // of bounds and TMA fills zeros
+        auto load_ids = [&](const Item &X, int chunk) {
+            const int lb = chunk * 32 + lane;
+            int coord = p.num_blocks;
+            if (X.live && X.valid && lb < X.nb) {
+                const int32_t blk = __ldg(p.block_tables + (int64_t)X.s * p.max_blocks + lb);
+                if (blk >= 0 && blk < p.num_blocks) coord = blk;
+                else set_status(p.status, PA_ERR_OUT_OF_RANGE);
+            }
+            return coord;
+        };
         Item I, I_next;
         ok = publish(0, I);
+        // the first two chunks of block ids are read one item ahead, when the
+        // item is published, so an item's first K copy waits on no table read
+        int pre_cur = load_ids(I, 0), pre_next = load_ids(I, 1);
         for (int it = 0; ok && I.live; ++it, I = I_next) {
             if (!publish(it + 1, I_next)) { ok = false; break; }
+            int ids_cur = pre_cur, ids_next = pre_next, chunk_cur = 0;
+            pre_cur = load_ids(I_next, 0);
+            pre_next = load_ids(I_next, 1);
             if (!I.valid) {
                 if (lane == 0) set_status(p.status, PA_ERR_OUT_OF_RANGE);
                 continue;
@@ -390,26 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
             ++nq;
-            // block ids, 32 per chunk (lane l holds block 32*chunk + l), one chunk ahead;
-            // past the sequence end (or invalid) the coordinate num_blocks is out of
-            // bounds and TMA fills zeros
-            const int32_t *bt = p.block_tables + (int64_t)I.s * p.max_blocks;
-            auto load_ids = [&](int chunk) {
-                const int lb = chunk * 32 + lane;
-                int coord = p.num_blocks;
-                if (lb < I.nb) {
-                    const int32_t blk = __ldg(bt + lb);
-                    if (blk >= 0 && blk < p.num_blocks) coord = blk;
-                    else set_status(p.status, PA_ERR_OUT_OF_RANGE);
-                }
-                return coord;
-            };
-            int ids_cur = load_ids(0), ids_next = load_ids(1), chunk_cur = 0;
             for (int j = 0; ok && j < I.nkv; ++j) {
                 if ((j * kBlocksPerTile) / 32 != chunk_cur) {
                     ids_cur = ids_next;
                     ++chunk_cur;
-                    ids_next = load_ids(chunk_cur + 1);
+                    ids_next = load_ids(I, chunk_cur + 1);
                 }
                 const int id0 = (j * kBlocksPerTile) & 31;
                 const int cbv = __shfl_sync(kFull, ids_cur, id0 + (lane & (kBlocksPerTile - 1)));
